@@ -1,0 +1,366 @@
+"""Plain, slow, fp64 definitions of softmax attention and of the tiled method.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the product path never
+imports this module.
+
+Conventions (the plainest reading where the pages leave a point open):
+
+* Tensors are ``[B, H, N, d]`` float64 arrays (the pages slice queries as
+  ``q[:, :, i:i+block]``, [P3] section 4). Queries and keys have the same
+  length N ([P3] appendix, "n here is one length, not two").
+* Grouped-query attention: query head ``hq`` reads key/value head
+  ``hq // G`` with ``G = Hq // Hkv`` (contiguous groups). The pages mention GQA
+  only for Llama's head counts ([P3] section 6); this mapping is a reading.
+* Causal: query ``i`` sees keys ``0..i`` inclusive; scores above the diagonal
+  become minus infinity ([P3] section 5).
+* The per-row statistic saved for the backward pass is the natural-log
+  log-sum-exp ``LSE_i = m_i + ln(l_i)`` of the scaled scores. [P3] section 8
+  says only "the saved statistics"; LSE is the one scalar that lets P be
+  recomputed as ``exp(S - LSE)``.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# --------------------------------------------------------------------------
+# Standard attention (the definition the method must reproduce exactly).
+# --------------------------------------------------------------------------
+
+
+def _kv_head(hq: int, Hq: int, Hkv: int) -> int:
+    """Key/value head read by query head ``hq`` (contiguous GQA groups)."""
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return hq // (Hq // Hkv)
+
+
+def _causal_mask(n_q: int, n_k: int, q_start: int = 0, k_start: int = 0) -> np.ndarray:
+    """Boolean mask, True where key position > query position (the future).
+
+    [P3] section 5: causal attention forces the scores above the diagonal to
+    minus infinity so the softmax gives them weight zero.
+    """
+    qi = np.arange(q_start, q_start + n_q)[:, None]
+    kj = np.arange(k_start, k_start + n_k)[None, :]
+    return kj > qi
+
+
+def attention_probs(q: np.ndarray, k: np.ndarray, causal: bool, scale: float) -> np.ndarray:
+    """Row-softmax weights P for ONE head: q [N,d], k [N,d] -> P [N,N].
+
+    Numerically stable softmax with the row max subtracted ([P3] section 2,
+    [P1] "The Running Statistics"): ``P_ij = exp(S_ij - m_i) / sum_j exp(S_ij - m_i)``.
+    """
+    S = scale * (q @ k.T)
+    if causal:
+        S = np.where(_causal_mask(q.shape[0], k.shape[0]), -np.inf, S)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    return P / P.sum(axis=1, keepdims=True)
+
+
+def attention_forward_head(q, k, v, causal: bool, scale: float):
+    """Standard attention for one head, fully materialised ([P3] section 1).
+
+    ``S = scale * Q K^T``; masked if causal; ``m = rowmax(S)``;
+    ``P = exp(S - m)``; ``l = rowsum(P)``; ``O = (P / l) V``; ``LSE = m + ln l``.
+    Returns ``(O [N,d], LSE [N])``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    S = scale * (q @ k.T)
+    if causal:
+        S = np.where(_causal_mask(q.shape[0], k.shape[0]), -np.inf, S)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    l = P.sum(axis=1, keepdims=True)
+    O = (P / l) @ v
+    lse = m[:, 0] + np.log(l[:, 0])
+    return O, lse
+
+
+def attention_forward(q, k, v, causal: bool, scale: float):
+    """Standard attention over ``[B,Hq,N,d]`` / ``[B,Hkv,N,d]`` arrays.
+
+    Head by head (to bound memory); returns ``(O [B,Hq,N,d], LSE [B,Hq,N])``.
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    O = np.empty((B, Hq, N, v.shape[3]), dtype=np.float64)
+    lse = np.empty((B, Hq, N), dtype=np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            hk = _kv_head(h, Hq, Hkv)
+            O[b, h], lse[b, h] = attention_forward_head(q[b, h], k[b, hk], v[b, hk], causal, scale)
+    return O, lse
+
+
+def attention_rows(q_rows, k, v, rows, causal: bool, scale: float):
+    """Standard attention for SELECTED query rows of one head.
+
+    ``q_rows`` [R,d] holds the queries at absolute positions ``rows`` (for the
+    causal mask); ``k``, ``v`` [N,d] hold every key of the head. Used where the
+    full N x N matrix is too large for the CPU, e.g. N = 131072.
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    rows = np.asarray(rows)
+    S = scale * (q_rows @ k.T)
+    if causal:
+        S = np.where(np.arange(k.shape[0])[None, :] > rows[:, None], -np.inf, S)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    l = P.sum(axis=1, keepdims=True)
+    return (P / l) @ v, m[:, 0] + np.log(l[:, 0])
+
+
+# --------------------------------------------------------------------------
+# Backward pass.
+# --------------------------------------------------------------------------
+
+
+def attention_backward_head(q, k, v, do, causal: bool, scale: float):
+    """Gradients of standard attention for one head.
+
+    [P3] section 8 ("One more piece: the backward pass") says only that the
+    probabilities are recomputed from Q, K, V and the saved statistics. The
+    gradient itself is the textbook one for ``O = softmax(scale Q K^T) V``:
+    ``dV = P^T dO``; ``dP = dO V^T``; ``delta = rowsum(dO * O)``;
+    ``dS = P * (dP - delta)``; ``dQ = scale dS K``; ``dK = scale dS^T Q``.
+    Returns ``(dQ, dK, dV)`` for this head.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    P = attention_probs(q, k, causal, scale)
+    O = P @ v
+    dV = P.T @ do
+    dP = do @ v.T
+    delta = np.sum(do * O, axis=1, keepdims=True)
+    dS = P * (dP - delta)
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q)
+    return dQ, dK, dV
+
+
+def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):
+    """Gradients over ``[B,Hq,N,d]`` arrays; dK, dV summed over each GQA group.
+
+    ``heads`` optionally restricts the computation to a list of ``(b, hkv)``
+    groups (the other entries of the returned arrays are NaN), for configs
+    whose full backward is too slow on the CPU.
+    """
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    groups = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hkv)]
+    for b, hk in groups:
+        dk[b, hk] = 0.0
+        dv[b, hk] = 0.0
+        for hq in range(hk * G, (hk + 1) * G):
+            gq, gk, gv = attention_backward_head(q[b, hq], k[b, hk], v[b, hk], do[b, hq], causal, scale)
+            dq[b, hq] = gq
+            dk[b, hk] += gk
+            dv[b, hk] += gv
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# Brute force (explicit loops, no matrix products) for tiny inputs.
+# --------------------------------------------------------------------------
+
+
+def brute_force_attention(q, k, v, causal: bool, scale: float):
+    """Softmax attention by explicit scalar loops (one head, small N only).
+
+    Written straight from the softmax definition of [P1] ("Here's the
+    challenge") without the max shift: ``w_ij = e^{s_ij} / sum_j e^{s_ij}``.
+    Returns ``(O, LSE)`` as nested Python lists of floats.
+    """
+    N, d = len(q), len(q[0])
+    dv = len(v[0])
+    O, lse = [], []
+    for i in range(N):
+        keys = range(i + 1) if causal else range(N)
+        s = {}
+        for j in keys:
+            acc = 0.0
+            for t in range(d):
+                acc += float(q[i][t]) * float(k[j][t])
+            s[j] = scale * acc
+        z = sum(math.exp(s[j]) for j in keys)
+        row = []
+        for c in range(dv):
+            row.append(sum(math.exp(s[j]) / z * float(v[j][c]) for j in keys))
+        O.append(row)
+        lse.append(math.log(z))
+    return O, lse
+
+
+# --------------------------------------------------------------------------
+# The online softmax and the tiled loop, step by step as the pages state them.
+# --------------------------------------------------------------------------
+
+
+def online_softmax(x, block_size: int):
+    """Single-pass online normaliser over the last axis ([P3] section 2, [P1]).
+
+    Carries a running max ``m`` and running sum ``l``. For each block:
+    ``m_new = max(m_old, max(block))``; ``correction = exp(m_old - m_new)``;
+    ``l = l * correction + sum(exp(block - m_new))``.
+    A second pass then forms ``exp(x - m) / l``.
+
+    Returns a dict: ``p`` (probabilities, same shape as x), ``m``, ``l``,
+    ``lse`` (= m + ln l), ``trace`` (per block: m, correction, l for the
+    first row) and ``rescales`` (per row: how many blocks moved the max,
+    counting the first block).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    lead = x.shape[:-1]
+    n = x.shape[-1]
+    m = np.full(lead + (1,), -np.inf)
+    l = np.zeros(lead + (1,))
+    rescales = np.zeros(lead, dtype=np.int64)
+    trace = []
+    for start in range(0, n, block_size):
+        block = x[..., start:start + block_size]
+        m_new = np.maximum(m, block.max(axis=-1, keepdims=True))
+        with np.errstate(invalid="ignore"):
+            correction = np.exp(m - m_new)
+        correction = np.where(np.isneginf(m), 0.0, correction)
+        rescales += (m_new > m)[..., 0]
+        l = l * correction + np.exp(block - m_new).sum(axis=-1, keepdims=True)
+        m = m_new
+        first = (0,) * len(lead)
+        trace.append({"m": float(m[first + (0,)]), "correction": float(correction[first + (0,)]),
+                      "l": float(l[first + (0,)])})
+    p = np.exp(x - m) / l
+    return {"p": p, "m": m[..., 0], "l": l[..., 0], "lse": m[..., 0] + np.log(l[..., 0]),
+            "trace": trace, "rescales": rescales}
+
+
+def tiled_attention(q, k, v, causal: bool, scale: float, block_q: int, block_k: int):
+    """The tiled two-level loop of [P3] section 4, in fp64, for one head.
+
+    Outer loop over query blocks of ``block_q`` rows; inner loop over key/value
+    blocks of ``block_k`` rows. Per query row: running max ``m``, running sum
+    ``l`` and accumulator ``acc``; per tile
+    ``m_new = max(m, rowmax(s))``, ``c = exp(m - m_new)``, ``p = exp(s - m_new)``,
+    ``l = l c + rowsum(p)``, ``acc = acc c + p V_j``; after the inner loop
+    ``O = acc / l``. With ``causal``, a tile whose first key lies after the
+    block's last query is skipped ([P3] section 7) and diagonal tiles are
+    masked element-wise ([P3] section 5).
+
+    Returns ``(O, LSE, counters)``; counters follow [P3] section 8's tallies
+    (two matmuls of ``2 rows cols d`` FLOPs per computed tile; K and V tile
+    reads of ``rows`` ... ``cols d`` elements) plus tile and rescale counts.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n_q, d = q.shape
+    n_k = k.shape[0]
+    O = np.empty((n_q, v.shape[1]))
+    lse = np.empty(n_q)
+    counters = {"tiles_computed": 0, "tiles_skipped": 0, "matmul_flops": 0,
+                "kv_elements_read": 0, "rescales": 0}
+    for i in range(0, n_q, block_q):
+        qi = q[i:i + block_q]
+        rows = qi.shape[0]
+        m = np.full((rows, 1), -np.inf)
+        l = np.zeros((rows, 1))
+        acc = np.zeros((rows, v.shape[1]))
+        for j in range(0, n_k, block_k):
+            if causal and j > i + rows - 1:
+                counters["tiles_skipped"] += 1
+                continue
+            kj, vj = k[j:j + block_k], v[j:j + block_k]
+            cols = kj.shape[0]
+            counters["tiles_computed"] += 1
+            counters["matmul_flops"] += 2 * (2 * rows * cols * d)
+            counters["kv_elements_read"] += 2 * cols * d
+            s = scale * (qi @ kj.T)
+            if causal:
+                s = np.where(_causal_mask(rows, cols, i, j), -np.inf, s)
+            m_new = np.maximum(m, s.max(axis=1, keepdims=True))
+            with np.errstate(invalid="ignore"):
+                c = np.exp(m - m_new)
+            c = np.where(np.isneginf(m), 0.0, c)
+            counters["rescales"] += int(np.sum((m_new > m) & ~np.isneginf(m)))
+            p = np.exp(s - m_new)
+            l = l * c + p.sum(axis=1, keepdims=True)
+            acc = acc * c + p @ vj
+            m = m_new
+        O[i:i + rows] = acc / l
+        lse[i:i + rows] = m[:, 0] + np.log(l[:, 0])
+    return O, lse, counters
+
+
+# --------------------------------------------------------------------------
+# Counts (no timing): tiles, FLOPs and HBM bytes as [P3] sections 7-8 tally them.
+# --------------------------------------------------------------------------
+
+
+def tile_schedule_counts(n: int, block_q: int, block_k: int, causal: bool,
+                         batch: int = 1, heads: int = 1, dim: int = 64, elem: int = 4):
+    """Walk the tiled loop's schedule without arithmetic and tally it.
+
+    Counts per [P3] section 7 (skip rule ``j > i + rows - 1``) and section 8:
+    ``matmul_flops += 2 (2 b h rows cols d)`` and
+    ``hbm_bytes += 2 b h cols d elem`` per computed tile, plus one read of Q
+    and one write of O (``2 b h n d elem``) for the all-tensor traffic total.
+    """
+    computed = skipped = flops = kv_bytes = 0
+    for i in range(0, n, block_q):
+        rows = min(block_q, n - i)
+        for j in range(0, n, block_k):
+            cols = min(block_k, n - j)
+            if causal and j > i + rows - 1:
+                skipped += 1
+                continue
+            computed += 1
+            flops += 2 * (2 * batch * heads * rows * cols * dim)
+            kv_bytes += 2 * batch * heads * cols * dim * elem
+    qo_bytes = 2 * batch * heads * n * dim * elem
+    return {"computed": computed, "skipped": skipped, "matmul_flops": flops,
+            "hbm_bytes": kv_bytes + qo_bytes}
+
+
+def naive_counts(n: int, batch: int = 1, heads: int = 1, dim: int = 64, elem: int = 4):
+    """Standard attention's counts ([P3] sections 1 and 8).
+
+    FLOPs: the two matmuls over the whole matrix, ``2 (2 b h n n d)``.
+    Score traffic: S written, read, P written, read: ``4 b h n^2 elem``.
+    All-tensor traffic adds Q, K, V reads and the O write: ``4 b h n d elem``.
+    """
+    flops = 2 * (2 * batch * heads * n * n * dim)
+    score = 4 * batch * heads * n * n * elem
+    return {"matmul_flops": flops, "score_bytes": score,
+            "hbm_bytes": score + 4 * batch * heads * n * dim * elem}
+
+
+def causal_tile_counts(n: int, block: int):
+    """(computed, skipped) square tiles for causal attention ([P3] section 7)."""
+    c = tile_schedule_counts(n, block, block, True)
+    return c["computed"], c["skipped"]
+
+
+def algorithmic_flops(B: int, Hq: int, N: int, d: int, causal: bool) -> int:
+    """Forward matmul FLOPs counted over VISIBLE (query, key) pairs only.
+
+    Each visible pair costs one multiply-add in ``Q K^T`` and one in ``P V``
+    per head-dimension element: ``4 d`` FLOPs ([P3] section 8's 2-per-MAC
+    convention). Non-causal: ``4 N^2 d`` per head; causal:
+    ``4 d N (N+1) / 2``.
+    """
+    pairs = N * (N + 1) // 2 if causal else N * N
+    return 4 * d * pairs * B * Hq
