@@ -1,0 +1,122 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact softmax attention library (libfa.so).
+ *
+ * Operation. For every batch b and query head hq, with kv head hkv = hq / (Hq/Hkv):
+ *     S = scale * Q K^T            (N x N, never stored)
+ *     S[i][j] = -inf for j > i     (only when causal != 0)
+ *     O = softmax_rows(S) V,  LSE_i = log(sum_j exp(S_ij))   (natural log)
+ * computed tile by tile with a running max m, running sum l and a rescaled output
+ * accumulator ("FlashAttention Implementation > How FlashAttention Uses Tiling",
+ * sections "The Running Statistics" and "Why the Correction Factor Works";
+ * "LLM Architecture Refresh [3]: Flash Attention Is Exact", sections 2 and 4).
+ * Key/value tiles lying wholly in a query tile's causal future are skipped, not masked
+ * (same post, section 7). The backward pass recomputes P from Q, K, V and LSE instead
+ * of storing it (same post, section 8, "One more piece: the backward pass").
+ *
+ * Layout. All tensors are dense, row-major and contiguous:
+ *     q, o, dout, dq : [B][Hq ][N][d]   bfloat16 (2 bytes, IEEE bfloat16 bit pattern)
+ *     k, v, dk, dv   : [B][Hkv][N][d]   bfloat16
+ *     lse            : [B][Hq ][N]      float32
+ * Supported: d in {64, 128}; N >= 1 (any value, not only multiples of 128); B, Hq, Hkv >= 1;
+ * Hq % Hkv == 0. Every pointer is a DEVICE pointer on the current CUDA device and must be
+ * 16-byte aligned.
+ *
+ * Ownership. The caller allocates and owns every buffer, including the backward
+ * workspace; the library never allocates device memory.
+ *
+ * Streams and errors. `stream` is a cudaStream_t (NULL = legacy default stream). Every call
+ * is asynchronous on that stream. The return value reports argument errors (nothing is
+ * launched) and launch errors synchronously. A device-side failure (a pipeline wait that
+ * exceeded its time limit; the kernel then stops early and its outputs are undefined) is
+ * recorded in a per-device status word and reported by fa_check(), which synchronises the
+ * stream. No call traps, asserts or spins without bound on the device.
+ *
+ * scale <= 0 (or NaN) selects the default 1/sqrt(d) ("LLM Architecture Refresh [3]",
+ * section 5, sliding_window_attention's scale).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,     /* null pointer, non-positive size, Hq % Hkv != 0, size overflow */
+  FA_ERR_UNSUPPORTED = -2, /* head dimension d not in {64, 128} */
+  FA_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+  FA_ERR_LAUNCH = -4,      /* CUDA launch or runtime error (see cudaGetLastError) */
+  FA_ERR_TIMEOUT = -5,     /* a device pipeline wait exceeded its limit; outputs undefined */
+  FA_ERR_WORKSPACE = -6,   /* workspace pointer null or smaller than fa_bwd_workspace_bytes() */
+  FA_ERR_DEVICE = -7       /* current device is not an sm_103 GPU (this library is sm_103a only) */
+} fa_status;
+
+/*
+ * Forward pass. Writes o (bf16) and lse (fp32, natural log).
+ * Source: "LLM Architecture Refresh [3]", section 4 (tiled loop, O = acc / l after the
+ * inner loop) and section 7 (causal tile skipping); LSE = m + ln(l) is the saved statistic
+ * that the backward pass needs (section 8).
+ * Extra device memory: none.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
+ * Same as fa_fwd, and additionally adds to counters[0..2] (device pointer to three
+ * unsigned 64-bit integers, which the caller zeroes): [0] key/value tiles computed,
+ * [1] key/value tiles skipped by the causal rule, [2] query rows whose running max was
+ * raised by a later tile (a rescale of l and O; "LLM Architecture Refresh [3]",
+ * section 2, "How often does it fire?"). Tiles are 128 x 128.
+ */
+int fa_fwd_stats(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 unsigned long long *counters, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator, the per-row
+ * delta = rowsum(dO * O) and the base-2 LSE, each over rows padded to a multiple of 128.
+ * Grows as O(B * Hq * N * d): never with N^2. Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+
+/*
+ * Backward pass: given q, k, v, the forward output o, its gradient dout and lse from
+ * fa_fwd (same causal and scale), writes dq, dk, dv (bf16). dk and dv are summed over the
+ * Hq/Hkv query heads that share a kv head. P is recomputed tile by tile as
+ * exp(scale * q k^T - lse) ("LLM Architecture Refresh [3]", section 8), then
+ *     dV = P^T dO,  dP = dO V^T,  delta = rowsum(dO * O),  dS = P * (dP - delta),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * workspace: device buffer of at least fa_bwd_workspace_bytes() bytes, 16-byte aligned;
+ * its contents on entry do not matter. dq is not deterministic bit for bit (fp32 atomics).
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+           const float *lse, void *dq, void *dk, void *dv,
+           void *workspace, size_t workspace_bytes,
+           int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status word:
+ * FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting) or FA_ERR_LAUNCH (the stream reported
+ * a CUDA error).
+ */
+int fa_check(fa_stream_t stream);
+
+/* Static, human-readable description of a status code. */
+const char *fa_strerror(int status);
+
+/* ABI version: (major << 16) | minor. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

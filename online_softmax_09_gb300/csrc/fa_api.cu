@@ -1,0 +1,247 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA descriptors, launch.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// Per-device status word written by kernels whose pipeline waits time out.
+__device__ uint32_t g_fa_status;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  uint32_t* status = nullptr;  // device address of g_fa_status on this device
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Looks up (once per device, with that device current) whether it is an sm_103 part and the
+// device address of its status word.
+int current_device(uint32_t** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
+      s.status = static_cast<uint32_t*>(addr);
+    }
+    s.init = true;
+  }
+  if (!s.supported) return FA_ERR_DEVICE;
+  if (status) *status = s.status;
+  return FA_OK;
+}
+
+bool load_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 3-D map over a [planes][N][d] bf16 tensor; box = 64 columns (128 B, one swizzle span) x 128
+// rows x 1 plane, 128-byte swizzle. Rows past N read as zero.
+int make_map(CUtensorMap* m, const void* base, int d, int N, long long planes) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
+}
+
+int check_sizes(int B, int Hq, int Hkv, int N, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID;
+  if (Hq % Hkv != 0) return FA_ERR_INVALID;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long tiles = (long long)B * Hq * ((N + fa::kTile - 1) / fa::kTile);
+  if (tiles > 0x7fffffffLL) return FA_ERR_INVALID;
+  if ((long long)B * Hq > 0x7fffffffLL) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+int check_ptr(const void* p) {
+  if (p == nullptr) return FA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+float resolve_scale(float scale, int d) { return (scale > 0.f) ? scale : 1.0f / std::sqrt((float)d); }
+
+struct WorkspaceLayout {
+  size_t dq_acc, delta, lse2, total;
+};
+WorkspaceLayout workspace_layout(int B, int Hq, int N, int d) {
+  const size_t rows = (size_t)B * Hq * fa::round_up_tile(N);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  WorkspaceLayout w;
+  w.dq_acc = 0;
+  w.delta = up(rows * d * 4);
+  w.lse2 = w.delta + up(rows * 4);
+  w.total = w.lse2 + up(rows * 4);
+  return w;
+}
+
+#define FA_TRY(x)               \
+  do {                          \
+    int _r = (x);               \
+    if (_r != FA_OK) return _r; \
+  } while (0)
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  FA_TRY(check_ptr(q));
+  FA_TRY(check_ptr(k));
+  FA_TRY(check_ptr(v));
+  FA_TRY(check_ptr(o));
+  FA_TRY(check_ptr(lse));
+  if (counters != nullptr && (reinterpret_cast<uintptr_t>(counters) & 7u)) return FA_ERR_ALIGN;
+  uint32_t* status = nullptr;
+  FA_TRY(current_device(&status));
+  if (!load_encoder()) return FA_ERR_LAUNCH;
+  CUtensorMap tq, tk, tv;
+  FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
+  FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
+  FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
+  fa::FwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.counters = counters;
+  a.status = status;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = resolve_scale(scale, d);
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return fa::launch_fwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+           int d, int causal, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream);
+}
+
+int fa_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                 int N, int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
+  if (counters == nullptr) return FA_ERR_INVALID;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, counters, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d) != FA_OK) return 0;
+  return workspace_layout(B, Hq, N, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+           int N, int d, int causal, float scale, fa_stream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+  for (const void* p : ptrs) FA_TRY(check_ptr(p));
+  const WorkspaceLayout w = workspace_layout(B, Hq, N, d);
+  if (workspace == nullptr || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
+  uint32_t* status = nullptr;
+  FA_TRY(current_device(&status));
+  if (!load_encoder()) return FA_ERR_LAUNCH;
+  CUtensorMap tq, tk, tv, tdo;
+  FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
+  FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
+  FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
+  FA_TRY(make_map(&tdo, dout, d, N, (long long)B * Hq));
+  char* ws = static_cast<char*>(workspace);
+  fa::BwdLaunch a;
+  a.tm_q = &tq;
+  a.tm_k = &tk;
+  a.tm_v = &tv;
+  a.tm_do = &tdo;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+  a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.status = status;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.causal = causal ? 1 : 0;
+  a.scale = resolve_scale(scale, d);
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  return fa::launch_bwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_check(fa_stream_t stream) {
+  uint32_t* status = nullptr;
+  int r = current_device(&status);
+  if (r != FA_OK) return r;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_LAUNCH;
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (h != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_LAUNCH;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument (null pointer, size < 1, Hq % Hkv != 0 or size overflow)";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension (d must be 64 or 128)";
+    case FA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case FA_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case FA_ERR_TIMEOUT: return "a device pipeline wait exceeded its time limit; outputs are undefined";
+    case FA_ERR_WORKSPACE: return "backward workspace missing or smaller than fa_bwd_workspace_bytes()";
+    case FA_ERR_DEVICE: return "current device is not an sm_103 (GB300) GPU";
+    default: return "unknown status";
+  }
+}
+
+int fa_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

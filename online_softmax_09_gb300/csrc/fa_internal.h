@@ -1,0 +1,49 @@
+// fa_internal.h -- host-side interface between the C ABI (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+constexpr int kTile = 128;  // query rows and key rows per tile (B_r = B_c = 128)
+
+struct FwdLaunch {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  void* o;
+  float* lse;
+  unsigned long long* counters;  // nullable
+  uint32_t* status;
+  int B, Hq, Hkv, N, d, causal;
+  float scale;
+  cudaStream_t stream;
+};
+cudaError_t launch_fwd(const FwdLaunch& a);
+
+struct BwdLaunch {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  const CUtensorMap* tm_do;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;   // workspace: [B*Hq][Npad][d] fp32
+  float* delta;    // workspace: [B*Hq][Npad] fp32
+  float* lse2;     // workspace: [B*Hq][Npad] fp32 (LSE * log2 e; +inf on padded rows)
+  uint32_t* status;
+  int B, Hq, Hkv, N, d, causal;
+  float scale;
+  cudaStream_t stream;
+};
+cudaError_t launch_bwd(const BwdLaunch& a);
+
+inline int round_up_tile(int n) { return (n + kTile - 1) / kTile * kTile; }
+
+}  // namespace fa

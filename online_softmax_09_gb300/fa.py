@@ -1,0 +1,131 @@
+"""Thin ctypes binding over libfa.so (include/fa.h). Argument marshalling only.
+
+Every step of attention runs in the library's CUDA kernels; this module only checks
+tensor metadata, allocates outputs with torch and passes raw device pointers and the
+current CUDA stream. There is no fallback: if libfa.so is missing or the GPU is not an
+sm_103 part, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({strerror(status)})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so once (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m online_softmax_09_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_fwd.restype = _i
+        L.fa_fwd_stats.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp]
+        L.fa_fwd_stats.restype = _i
+        L.fa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_bwd.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_bwd.restype = _i
+        L.fa_check.argtypes = [_vp]
+        L.fa_check.restype = _i
+        L.fa_strerror.argtypes = [_i]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_version.argtypes = []
+        L.fa_version.restype = _i
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def _stream_handle(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _check_qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor [B, H, N, d]")
+    B, Hq, N, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError("k and v must be [B, Hkv, N, d] with the same B, N, d as q")
+    return B, Hq, k.shape[1], N, d
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            stream=None, counters=None):
+    """O, LSE = attention(q, k, v). q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 CUDA tensors."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    h = _stream_handle(stream, q.device)
+    if counters is None:
+        r = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                         B, Hq, Hkv, N, d, int(bool(causal)), sc, h)
+    else:
+        r = lib().fa_fwd_stats(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                               B, Hq, Hkv, N, d, int(bool(causal)), sc, counters.data_ptr(), h)
+    if r != FA_OK:
+        raise FAError(r, "fa_fwd")
+    return o, l
+
+
+def workspace_bytes(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of attention given the forward's o and lse and the output gradient do."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must match q")
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    nbytes = workspace_bytes(B, Hq, Hkv, N, d)
+    ws = workspace if workspace is not None else torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+                     B, Hq, Hkv, N, d, int(bool(causal)), sc, _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_bwd")
+    return dq, dk, dv
+
+
+def check(stream=None, device=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a device-side failure."""
+    dev = device if device is not None else torch.cuda.current_device()
+    r = lib().fa_check(_stream_handle(stream, dev))
+    if r != FA_OK:
+        raise FAError(r, "fa_check")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

@@ -1,0 +1,73 @@
+"""The C-ABI library builds, loads and exports every function include/fa.h declares.
+
+No GPU needed: only argument checks that return before any CUDA call are exercised.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from online_softmax_09_gb300 import build, fa
+
+    build.build()
+    return fa.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*\*?\s*(fa_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_stats", "fa_check", "fa_strerror", "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    from online_softmax_09_gb300 import fa
+
+    for s in range(0, -8, -1):
+        assert fa.strerror(s) and fa.strerror(s) != "unknown status"
+    assert fa.strerror(-99) == "unknown status"
+    assert L.fa_version() >> 16 == 1
+
+
+def _fwd(L, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, Hq=1, Hkv=1, N=128, d=128):
+    return L.fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, 0, 0.0, None)
+
+
+def test_argument_errors_return_before_any_launch(L):
+    assert _fwd(L, q=None) == -1  # null pointer
+    assert _fwd(L, N=0) == -1
+    assert _fwd(L, B=0) == -1
+    assert _fwd(L, Hq=3, Hkv=2) == -1  # Hq % Hkv != 0
+    assert _fwd(L, d=96) == -2  # unsupported head dim
+    assert _fwd(L, d=256) == -2
+    assert _fwd(L, k=0x1008) == -3  # misaligned
+    assert _fwd(L, lse=0x1004) == -3
+    assert L.fa_fwd_stats(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 1, 128, 128, 0, 0.0, None, None) == -1
+
+
+def test_workspace_size_is_linear_in_n(L):
+    ws = [L.fa_bwd_workspace_bytes(2, 8, 2, n, 128) for n in (1024, 2048, 4096)]
+    assert ws[2] - ws[1] == 2 * (ws[1] - ws[0])  # affine in N: no N^2 term
+    assert ws[0] >= 2 * 8 * 1024 * (128 + 2) * 4
+    assert L.fa_bwd_workspace_bytes(1, 3, 2, 128, 128) == 0  # invalid sizes
+    # Backward argument errors.
+    args = [0x1000] * 9
+    assert L.fa_bwd(*args, 0x1000, 0, 1, 1, 1, 128, 128, 0, 0.0, None) == -6  # workspace too small
+    assert L.fa_bwd(*args, None, 1 << 30, 1, 1, 1, 128, 128, 0, 0.0, None) == -6
+    assert L.fa_bwd(*args, 0x1001, 1 << 30, 1, 1, 1, 128, 128, 0, 0.0, None) == -3

@@ -299,3 +299,15 @@ def test_backward_head_subset():
     np.testing.assert_allclose(part[0][0, 2:], full[0][0, 2:])
     np.testing.assert_allclose(part[1][0, 1], full[1][0, 1])
     assert np.all(np.isnan(part[1][0, 0]))
+
+
+def test_half_ulp_bf16_matches_torch_rounding():
+    # The forward tolerance allows the bf16 output quantisation; check the helper's half-ulp
+    # bound against torch's own round-to-nearest bf16 conversion.
+    import torch
+    from gpu_util import half_ulp_bf16
+
+    x = np.concatenate([np.random.default_rng(30).standard_normal(20000) * s for s in (0.01, 1, 4, 100)])
+    r = torch.tensor(x).to(torch.bfloat16).double().numpy()
+    assert np.all(np.abs(r - x) <= half_ulp_bf16(np.maximum(np.abs(x), np.abs(r))) * (1 + 1e-12))
+    assert np.max(np.abs(r - x) / half_ulp_bf16(np.abs(x))) > 0.9  # the bound is tight
