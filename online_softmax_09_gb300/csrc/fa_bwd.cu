@@ -1,6 +1,545 @@
-// fa_bwd.cu -- backward pass (work in progress).
+// fa_bwd.cu -- backward pass of exact softmax attention on sm_103a.
+//
+// The forward pass kept only O and the per-row log-sum-exp; the probabilities are recomputed
+// tile by tile from Q, K, V and LSE instead of being stored ("LLM Architecture Refresh [3]:
+// Flash Attention Is Exact", section 8, "One more piece: the backward pass"). Gradients are
+// the textbook ones for O = softmax(scale Q K^T) V:
+//   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, delta = rowsum(dO * O),
+//   dS = P * (dP - delta), dQ = scale dS K, dK = scale dS^T Q.
+//
+// Three kernels on the caller's stream:
+//   1. preprocess: delta and LSE*log2(e) per query row (padded rows: 0 and +inf), and zeroes
+//      the fp32 dQ accumulator.                                               (HBM-bound)
+//   2. main: one CTA per (batch, kv head, 128-key tile). It keeps K_n and V_n in shared
+//      memory and the dK, dV accumulators in TMEM, and loops over the G query heads of its
+//      group and their query tiles (causal: from the diagonal tile on). Per query tile:
+//        MMA  dP^T = V_n dO_i^T   and   S^T = K_n Q_i^T          (smem x smem -> TMEM)
+//        softmax warps (thread = key row): P^T = 2^(S^T scale log2e - LSE2), bf16 -> TMEM
+//        MMA  dV += P^T dO_i                                     (TMEM x smem -> TMEM)
+//        softmax warps: dS^T = P^T (dP^T - delta), bf16 -> TMEM and -> shared memory
+//        MMA  dK += dS^T Q_i ;  dQ_i = dS K_n  (into the S^T columns, now free)
+//        drain warps (thread = query row): dQ_i TMEM -> fp32 red.global.add into the
+//        workspace accumulator.
+//   3. dQ conversion: dq = bf16(scale * accumulator).
+//
+// Warp roles of the main kernel: 0-3 softmax/dS and the final dK/dV epilogue, 4 TMA producer,
+// 5 MMA issuer and TMEM owner, 6-9 dQ drain.
+// TMEM columns: S^T/P^T/dQ [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D,256+2D).
+// For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
+// after the dV MMA (the last reader of dO) has completed; for D = 64 it has its own buffer.
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdLaunch&) { return cudaErrorNotSupported; }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------------------------------
+// 1. Preprocess: delta = rowsum(dO * O), LSE2 = LSE * log2(e), dQ accumulator = 0.
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dout,
+                                                         const float* __restrict__ lse, float* __restrict__ dq_acc,
+                                                         float* __restrict__ delta, float* __restrict__ lse2,
+                                                         int N, int Npad, long long rows) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
+  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long r = gt / TPR;  // row of the padded [B*Hq][Npad] grid
+  const int part = (int)(gt % TPR);
+  if (r >= rows) return;  // rows are whole TPR-lane groups, so groups exit together
+  const long long bh = r / Npad;
+  const int n = (int)(r - bh * Npad);
+  float4* acc = reinterpret_cast<float4*>(dq_acc + r * D + part * 8);
+  acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float s = 0.f;
+  if (n < N) {
+    const size_t off = ((size_t)bh * N + n) * D + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 dv = *reinterpret_cast<const uint4*>(dout + off);
+    const __nv_bfloat162* op = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* dp = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __bfloat1622float2(op[i]);
+      const float2 b = __bfloat1622float2(dp[i]);
+      s = fmaf(a.x, b.x, s);
+      s = fmaf(a.y, b.y, s);
+    }
+  }
+  const int lane = threadIdx.x & 31;
+  const unsigned group = ((TPR == 32) ? 0xffffffffu : ((1u << TPR) - 1u)) << (lane & ~(TPR - 1));
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(group, s, off);
+  if (part == 0) {
+    delta[r] = (n < N) ? s : 0.f;
+    lse2[r] = (n < N) ? lse[(size_t)bh * N + n] * kLog2e : INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// 3. dq = bf16(scale * dq_acc) on the unpadded rows.
+// ------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dq_acc,
+                                                        __nv_bfloat16* __restrict__ dq, int N, int Npad,
+                                                        long long n_vec4, float scale) {
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec4;
+       v += (long long)gridDim.x * blockDim.x) {
+    const long long e = v * 4;
+    const long long row = e / D;  // over [B*Hq][N]
+    const int col = (int)(e - row * D);
+    const long long bh = row / N;
+    const long long n = row - bh * N;
+    const float4 a = *reinterpret_cast<const float4*>(dq_acc + (bh * Npad + n) * D + col);
+    uint2 w;
+    w.x = pack_bf16(a.x * scale, a.y * scale);
+    w.y = pack_bf16(a.z * scale, a.w * scale);
+    *reinterpret_cast<uint2*>(dq + e) = w;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// 2. Main kernel.
+// ------------------------------------------------------------------------------------------
+struct BwdParams {
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* dq_acc;
+  const float* delta;
+  const float* lse2;
+  uint32_t* status;
+  int B, Hq, Hkv, N, Npad, causal, num_tiles;
+  float scale, scale_log2;
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr bool kAliasDS = (D == 128);
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kStage0 = kV + kTileBytes;
+  // Stage layout: Q tile, dO tile, LSE2 (128 fp32), delta (128 fp32).
+  static constexpr int kStQ = 0;
+  static constexpr int kStDO = kTileBytes;
+  static constexpr int kStL = 2 * kTileBytes;
+  static constexpr int kStD = 2 * kTileBytes + 512;
+  static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kDS = kStage0 + 2 * kStageBytes;
+  static constexpr int kBar = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
+  enum {
+    bKV = 0,
+    bQFull = 1,       // 2
+    bDOFull = 3,      // 2
+    bStageEmpty = 5,  // 2
+    bSFull = 7,
+    bDPFull,
+    bPReady,
+    bDSReady,
+    bDVDone,
+    bSmemDS,
+    bDQFull,
+    bDQFree,
+    bFinal,
+    bDrain,
+    kNumBars
+  };
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kStageBytes % 1024 == 0 && kStage0 % 1024 == 0 && kDS % 1024 == 0, "1024-byte alignment");
+};
+
+constexpr int kBwdThreads = 320;
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase + L::kK;
+  const uint32_t sV = sbase + L::kV;
+  auto stage = [&](int s) -> uint32_t { return sbase + L::kStage0 + (uint32_t)s * L::kStageBytes; };
+  auto stage_ptr = [&](int s) -> uint8_t* { return smem + L::kStage0 + s * L::kStageBytes; };
+  auto sDS = [&](int s) -> uint32_t { return L::kAliasDS ? stage(s) + L::kStDO : sbase + L::kDS; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  const Ctl ctl{abort_flag, p.status};
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBar + 8u * (uint32_t)i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: key tile n of kv head (b, hkv). Causal tiles with the most query tiles first.
+  const int BHk = p.B * p.Hkv;
+  const int n = blockIdx.x / BHk;
+  const int bhk = blockIdx.x - n * BHk;
+  const int b = bhk / p.Hkv;
+  const int hkv = bhk - b * p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const int n_i = p.causal ? (p.num_tiles - n) : p.num_tiles;
+  const int i0 = p.causal ? n : 0;
+  const int n_iter = G * n_i;
+  auto item = [&](int it, int& hq, int& i) {
+    const int g = it / n_i;
+    hq = hkv * G + g;
+    i = i0 + (it - g * n_i);
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::bKV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(L::bQFull + s), 1);
+      mbar_init(bar(L::bDOFull + s), 1);
+      mbar_init(bar(L::bStageEmpty + s), 1);
+    }
+    mbar_init(bar(L::bSFull), 1);
+    mbar_init(bar(L::bDPFull), 1);
+    mbar_init(bar(L::bPReady), 128);
+    mbar_init(bar(L::bDSReady), 128);
+    mbar_init(bar(L::bDVDone), 1);
+    mbar_init(bar(L::bSmemDS), 128);
+    mbar_init(bar(L::bDQFull), 1);
+    mbar_init(bar(L::bDQFree), 128);
+    mbar_init(bar(L::bFinal), 1);
+    mbar_init(bar(L::bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;         // S^T, then P^T (bf16), then dQ
+  const uint32_t tdP = tmem + 128;  // dP^T, then dS^T (bf16)
+  const uint32_t tdV = tmem + 256;
+  const uint32_t tdK = tmem + 256 + D;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      constexpr uint32_t kTB = L::kTileBytes;
+      const int kv_z = b * p.Hkv + hkv;
+      mbar_expect_tx(bar(L::bKV), 2 * kTB);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sK + c * 16384, &tm_k, bar(L::bKV), c * 64, n * kTile, kv_z);
+        tma_load_3d(sV + c * 16384, &tm_v, bar(L::bKV), c * 64, n * kTile, kv_z);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(bar(L::bStageEmpty + s), ((it >> 1) & 1) ^ 1, ctl)) break;
+        int hq, i;
+        item(it, hq, i);
+        const int qz = b * p.Hq + hq;
+        const size_t srow = (size_t)qz * p.Npad + (size_t)i * kTile;
+        const uint32_t st = stage(s);
+        mbar_expect_tx(bar(L::bQFull + s), kTB + 512);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(st + L::kStQ + c * 16384, &tm_q, bar(L::bQFull + s), c * 64, i * kTile, qz);
+        bulk_load(st + L::kStL, p.lse2 + srow, 512, bar(L::bQFull + s));
+        mbar_expect_tx(bar(L::bDOFull + s), kTB + 512);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(st + L::kStDO + c * 16384, &tm_do, bar(L::bDOFull + s), c * 64, i * kTile, qz);
+        bulk_load(st + L::kStD, p.delta + srow, 512, bar(L::bDOFull + s));
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        drain_wait(bar(L::bKV), 0);
+        for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
+          drain_wait(bar(L::bQFull + (it & 1)), (it >> 1) & 1);
+          drain_wait(bar(L::bDOFull + (it & 1)), (it >> 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
+      constexpr uint32_t idDQ = idesc_bf16_f32(128, D, true, true);      // dQ
+      bool ok = mbar_wait(bar(L::bKV), 0, ctl);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        const uint32_t sQ = stage(s) + L::kStQ;
+        const uint32_t sDO = stage(s) + L::kStDO;
+        // dP^T = V_n dO_i^T
+        if (!(ok = mbar_wait(bar(L::bDOFull + s), ph, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::bDPFull));
+        // S^T = K_n Q_i^T, once the previous dQ has been drained out of these columns.
+        if (!(ok = mbar_wait(bar(L::bQFull + s), ph, ctl))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::bSFull));
+        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand)
+        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tdV, tS + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+        mma_commit(bar(L::bDVDone));
+        // dK += dS^T Q_i
+        if (!(ok = mbar_wait(bar(L::bDSReady), it & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tdK, tdP + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+        // dQ_i = dS K_n  (dS and K both MN-major in shared memory) into the S^T columns
+        if (!(ok = mbar_wait(bar(L::bSmemDS), it & 1, ctl))) break;
+        tc_fence_after();
+        const uint32_t sds = sDS(s);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tS, sdesc_sw128(sds + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ,
+                 kk > 0);
+        mma_commit(bar(L::bDQFull));
+        mma_commit(bar(L::bStageEmpty + s));
+      }
+      if (ok) mma_commit(bar(L::bFinal));
+      if (*abort_flag) {
+        mma_commit(bar(L::bDrain));
+        drain_wait(bar(L::bDrain), 0);
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ softmax / dS warps
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int kr = threadIdx.x;  // key row within the tile
+    const int key = n * kTile + kr;
+    const bool key_ok = key < p.N;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      int hq, i;
+      item(it, hq, i);
+      const bool diag = p.causal && i == n;
+      const float* sl = reinterpret_cast<const float*>(stage_ptr(s) + L::kStL);
+      const float* sd = reinterpret_cast<const float*>(stage_ptr(s) + L::kStD);
+      if (!(ok = mbar_wait_warp(bar(L::bQFull + s), ph, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bSFull), it & 1, ctl))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(tS + lane_off + c * 32, sr);
+        tmem_ld_wait(sr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float pv[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int q = c * 32 + j + t;
+            pv[t] = ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
+            if (!key_ok || (diag && q < kr)) pv[t] = 0.f;
+          }
+          pk[j / 2] = pack_bf16(pv[0], pv[1]);
+          pk[j / 2 + 1] = pack_bf16(pv[2], pv[3]);
+        }
+        // P^T (bf16) overwrites S^T columns [16c, 16c+16), all of which were read already.
+        tmem_st16(tS + lane_off + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::bPReady));
+
+      if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), ph, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bDPFull), it & 1, ctl))) break;
+      tc_fence_after();
+      // dS^T = P^T (dP^T - delta), with P^T read back as the bf16 values the dV MMA uses.
+      uint32_t dsp[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dr[32];
+        uint32_t pr[16];
+        tmem_ld32(tdP + lane_off + c * 32, dr);
+        tmem_ld16(tS + lane_off + c * 16, pr);
+        tmem_ld_wait(dr);
+        tmem_ld_wait(pr);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sd + c * 32 + j);
+          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pr[j / 2]));
+          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pr[j / 2 + 1]));
+          dsp[c][j / 2] = pack_bf16(p01.x * (__uint_as_float(dr[j + 0]) - d4.x),
+                                    p01.y * (__uint_as_float(dr[j + 1]) - d4.y));
+          dsp[c][j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
+                                        p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
+        }
+        tmem_st16(tdP + lane_off + c * 16, dsp[c]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(L::bDSReady));
+
+      // dS (bf16) into shared memory as the MN-major A operand of the dQ MMA: row = key,
+      // 64-query chunks 16 KB apart, 16-byte granules XOR-swizzled by (key mod 8).
+      if (!(ok = mbar_wait_warp(bar(L::bDVDone), it & 1, ctl))) break;
+      const uint32_t row_base = sDS(s) + (uint32_t)kr * 128;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int pi = h * 32 + g * 4;  // packed pair index of query 64h + 8g
+          const uint32_t* src = &dsp[pi >> 4][pi & 15];
+          st_shared_v4(row_base + h * 16384 + ((g ^ (kr & 7)) << 4), src[0], src[1], src[2], src[3]);
+        }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::bSmemDS));
+    }
+    // ---------------------------------------------------------------- dK / dV epilogue
+    if (ok) ok = mbar_wait_warp(bar(L::bFinal), 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      const size_t row_off = ((size_t)(b * p.Hkv + hkv) * p.N + key) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t src = which ? tdK : tdV;
+        const float mul = which ? p.scale : 1.f;
+        __nv_bfloat16* dst_base = which ? p.dk : p.dv;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(src + lane_off + c * 32, a);
+          tmem_ld_wait(a);
+          uint4 w[4];
+          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = w[j];
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ drain warps 6-9
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int qr = (warp & 3) * 32 + lane;  // query row within the tile (TMEM lane)
+    for (int it = 0; it < n_iter; ++it) {
+      int hq, i;
+      item(it, hq, i);
+      if (!mbar_wait_warp(bar(L::bDQFull), it & 1, ctl)) break;
+      tc_fence_after();
+      uint32_t a[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tS + lane_off + c * 32, a[c]);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(a[c]);
+      tc_fence_before();
+      mbar_arrive(bar(L::bDQFree));
+      float* dst = p.dq_acc + ((size_t)(b * p.Hq + hq) * p.Npad + (size_t)i * kTile + qr) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          red_add_v4(dst + c * 32 + j, __uint_as_float(a[c][j]), __uint_as_float(a[c][j + 1]),
+                     __uint_as_float(a[c][j + 2]), __uint_as_float(a[c][j + 3]));
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const BwdLaunch& a) {
+  const int T = (a.N + kTile - 1) / kTile;
+  const int Npad = T * kTile;
+  const long long rows = (long long)a.B * a.Hq * Npad;
+  {
+    const long long threads = rows * (D / 8);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    fa_bwd_pre_kernel<D><<<blocks, 256, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.dq_acc,
+        a.delta, a.lse2, a.N, Npad, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    constexpr int smem = BwdSmem<D>::kAlloc;
+    static_assert(smem <= 232448, "backward shared memory exceeds the 227 KB per-CTA limit");
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    BwdParams p;
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    p.dq_acc = a.dq_acc;
+    p.delta = a.delta;
+    p.lse2 = a.lse2;
+    p.status = a.status;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.N = a.N;
+    p.Npad = Npad;
+    p.causal = a.causal;
+    p.num_tiles = T;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    const long long grid = (long long)a.B * a.Hkv * T;
+    fa_bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long n_vec4 = (long long)a.B * a.Hq * a.N * D / 4;
+    const long long want = (n_vec4 + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 152 * 32 ? want : 152 * 32);
+    fa_bwd_dq_kernel<D><<<blocks, 256, 0, a.stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.N, Npad,
+                                                      n_vec4, a.scale);
+    return cudaGetLastError();
+  }
+}
+
+cudaError_t launch_bwd(const BwdLaunch& a) {
+  if (a.d == 128) return launch_bwd_t<128>(a);
+  return launch_bwd_t<64>(a);
+}
+
 }  // namespace fa

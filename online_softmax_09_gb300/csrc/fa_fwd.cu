@@ -58,15 +58,6 @@ struct FwdSmem {
 constexpr int kFwdThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 
-// Bounded wait that ignores the abort flag: used only to let in-flight copies and MMAs land
-// before the CTA releases its shared and tensor memory.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
 template <int D, int NS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,

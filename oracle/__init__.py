@@ -30,6 +30,7 @@ from .attention import (  # noqa: F401
     algorithmic_flops,
     attention_backward,
     attention_backward_head,
+    attention_backward_rows,
     attention_forward,
     attention_forward_head,
     attention_probs,

@@ -364,3 +364,48 @@ def algorithmic_flops(B: int, Hq: int, N: int, d: int, causal: bool) -> int:
     """
     pairs = N * (N + 1) // 2 if causal else N * N
     return 4 * d * pairs * B * Hq
+
+
+def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: float, chunk: int = 1024):
+    """Backward of standard attention for ONE head, on selected rows only.
+
+    Returns ``(dQ[q_rows], dK[k_rows], dV[k_rows])`` without forming the N x N matrices:
+    the row statistics (LSE, delta) are computed over query chunks of ``chunk`` rows, then
+    ``dQ_i = scale sum_j P_ij (dP_ij - delta_i) K_j`` for the selected queries and
+    ``dV_j = sum_i P_ij dO_i``, ``dK_j = scale sum_i P_ij (dP_ij - delta_i) Q_i`` for the
+    selected keys, with ``P_ij = exp(scale q_i.k_j - LSE_i)`` and ``dP_ij = dO_i . v_j``.
+    Same definitions as :func:`attention_backward_head`, evaluated on a subset.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    N = q.shape[0]
+    lse = np.empty(N)
+    delta = np.empty(N)
+    for s in range(0, N, chunk):
+        rows = np.arange(s, min(N, s + chunk))
+        O_c, lse[rows] = attention_rows(q[rows], k, v, rows, causal, scale)
+        delta[rows] = np.sum(do[rows] * O_c, axis=1)
+    q_rows = np.asarray(q_rows)
+    k_rows = np.asarray(k_rows)
+    # dQ for the selected queries.
+    S = scale * (q[q_rows] @ k.T)
+    if causal:
+        S = np.where(np.arange(N)[None, :] > q_rows[:, None], -np.inf, S)
+    P = np.exp(S - lse[q_rows, None])
+    dS = P * (do[q_rows] @ v.T - delta[q_rows, None])
+    dQ = scale * (dS @ k)
+    # dK, dV for the selected keys.
+    dK = np.zeros((len(k_rows), q.shape[1]))
+    dV = np.zeros((len(k_rows), v.shape[1]))
+    for s in range(0, N, chunk):
+        rows = np.arange(s, min(N, s + chunk))
+        St = scale * (q[rows] @ k[k_rows].T)
+        if causal:
+            St = np.where(k_rows[None, :] > rows[:, None], -np.inf, St)
+        Pt = np.exp(St - lse[rows, None])
+        dSt = Pt * (do[rows] @ v[k_rows].T - delta[rows, None])
+        dV += Pt.T @ do[rows]
+        dK += scale * (dSt.T @ q[rows])
+    return dQ, dK, dV

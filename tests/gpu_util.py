@@ -88,6 +88,8 @@ def sample_rows(N, n_random, seed):
     return sorted(fixed | set(g.integers(0, N, size=n_random).tolist()))
 
 
-def rel_fro(x, ref):
+def rel_fro(x, ref, floor=0.0):
+    """||x - ref||_F / max(||ref||_F, floor). The floor matters only where the exact gradient
+    vanishes (e.g. N = 1, where the single weight is 1 and dQ = dK = 0 exactly)."""
     x = np.asarray(x, dtype=np.float64)
-    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), floor, 1e-300))

@@ -311,3 +311,16 @@ def test_half_ulp_bf16_matches_torch_rounding():
     r = torch.tensor(x).to(torch.bfloat16).double().numpy()
     assert np.all(np.abs(r - x) <= half_ulp_bf16(np.maximum(np.abs(x), np.abs(r))) * (1 + 1e-12))
     assert np.max(np.abs(r - x) / half_ulp_bf16(np.abs(x))) > 0.9  # the bound is tight
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_matches_full_backward(causal):
+    rng = _rng(24)
+    N, d = 70, 6
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    dq, dk, dv = oracle.attention_backward_head(q, k, v, do, causal, 0.4)
+    qr, kr = np.array([0, 5, 33, 69]), np.array([0, 1, 40, 69])
+    rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, qr, kr, causal, 0.4, chunk=16)
+    np.testing.assert_allclose(rq, dq[qr], atol=1e-12)
+    np.testing.assert_allclose(rk, dk[kr], atol=1e-12)
+    np.testing.assert_allclose(rv, dv[kr], atol=1e-12)
