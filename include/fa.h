@@ -103,6 +103,28 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
            fa_stream_t stream);
 
 /*
+ * The three stages fa_bwd runs, exposed so that a caller can schedule or time them apart.
+ * They must be called in this order on one stream with the same sizes and workspace;
+ * fa_bwd(...) is exactly prepare, compute, finalize.
+ *   fa_bwd_prepare : delta = rowsum(dout * o) and lse * log2(e) per query row into the
+ *                    workspace, and zeroes the workspace's fp32 dQ accumulator
+ *                    (memory-bound: reads o, dout, lse).
+ *   fa_bwd_compute : the recompute kernel: writes dk, dv and adds dQ contributions (before
+ *                    the final scale) into the workspace accumulator (reads q, k, v, dout).
+ *   fa_bwd_finalize: dq = bf16(scale * accumulator).
+ * Same argument meanings, layouts and errors as fa_bwd.
+ */
+int fa_bwd_prepare(const void *o, const void *dout, const float *lse,
+                   void *workspace, size_t workspace_bytes,
+                   int B, int Hq, int Hkv, int N, int d, fa_stream_t stream);
+int fa_bwd_compute(const void *q, const void *k, const void *v, const void *dout,
+                   void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                   int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                   fa_stream_t stream);
+int fa_bwd_finalize(void *dq, void *workspace, size_t workspace_bytes,
+                    int B, int Hq, int Hkv, int N, int d, float scale, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting) or FA_ERR_LAUNCH (the stream reported
  * a CUDA error).

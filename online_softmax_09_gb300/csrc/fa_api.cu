@@ -149,43 +149,32 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   return fa::launch_fwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-}  // namespace
-
-extern "C" {
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
-           int d, int causal, float scale, fa_stream_t stream) {
-  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream);
-}
-
-int fa_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                 int N, int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
-  if (counters == nullptr) return FA_ERR_INVALID;
-  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, counters, stream);
-}
-
-size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
-  if (check_sizes(B, Hq, Hkv, N, d) != FA_OK) return 0;
-  return workspace_layout(B, Hq, N, d).total;
-}
-
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
-           int N, int d, int causal, float scale, fa_stream_t stream) {
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
+             int d, int causal, float scale, fa_stream_t stream, int stages) {
   FA_TRY(check_sizes(B, Hq, Hkv, N, d));
-  const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
-  for (const void* p : ptrs) FA_TRY(check_ptr(p));
+  // Pointers each stage reads or writes.
+  if (stages & fa::kBwdPrepare) {
+    for (const void* p : {o, dout, static_cast<const void*>(lse)}) FA_TRY(check_ptr(p));
+  }
+  if (stages & fa::kBwdCompute) {
+    for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+      FA_TRY(check_ptr(p));
+  }
+  if (stages & fa::kBwdFinalize) FA_TRY(check_ptr(dq));
   const WorkspaceLayout w = workspace_layout(B, Hq, N, d);
   if (workspace == nullptr || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
   uint32_t* status = nullptr;
   FA_TRY(current_device(&status));
-  if (!load_encoder()) return FA_ERR_LAUNCH;
   CUtensorMap tq, tk, tv, tdo;
-  FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
-  FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
-  FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
-  FA_TRY(make_map(&tdo, dout, d, N, (long long)B * Hq));
+  if (stages & fa::kBwdCompute) {
+    if (!load_encoder()) return FA_ERR_LAUNCH;
+    FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
+    FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
+    FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
+    FA_TRY(make_map(&tdo, dout, d, N, (long long)B * Hq));
+  }
   char* ws = static_cast<char*>(workspace);
   fa::BwdLaunch a;
   a.tm_q = &tq;
@@ -210,7 +199,53 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   a.causal = causal ? 1 : 0;
   a.scale = resolve_scale(scale, d);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
-  return fa::launch_bwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return fa::launch_bwd(a, stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+           int d, int causal, float scale, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream);
+}
+
+int fa_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                 int N, int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
+  if (counters == nullptr) return FA_ERR_INVALID;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, counters, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d) != FA_OK) return 0;
+  return workspace_layout(B, Hq, N, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+           int N, int d, int causal, float scale, fa_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale,
+                  stream, fa::kBwdAll);
+}
+
+int fa_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace, size_t workspace_bytes,
+                   int B, int Hq, int Hkv, int N, int d, fa_stream_t stream) {
+  return bwd_impl(nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr, nullptr, workspace, workspace_bytes,
+                  B, Hq, Hkv, N, d, 0, 0.f, stream, fa::kBwdPrepare);
+}
+
+int fa_bwd_compute(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                   void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
+                   float scale, fa_stream_t stream) {
+  return bwd_impl(q, k, v, nullptr, dout, nullptr, nullptr, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d,
+                  causal, scale, stream, fa::kBwdCompute);
+}
+
+int fa_bwd_finalize(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
+                    float scale, fa_stream_t stream) {
+  return bwd_impl(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr, workspace,
+                  workspace_bytes, B, Hq, Hkv, N, d, 0, scale, stream, fa::kBwdFinalize);
 }
 
 int fa_check(fa_stream_t stream) {

@@ -488,11 +488,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <int D>
-static cudaError_t launch_bwd_t(const BwdLaunch& a) {
+static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
   const int T = (a.N + kTile - 1) / kTile;
   const int Npad = T * kTile;
   const long long rows = (long long)a.B * a.Hq * Npad;
-  {
+  if (stages & kBwdPrepare) {
     const long long threads = rows * (D / 8);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     fa_bwd_pre_kernel<D><<<blocks, 256, 0, a.stream>>>(
@@ -501,7 +501,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (stages & kBwdCompute) {
     constexpr int smem = BwdSmem<D>::kAlloc;
     static_assert(smem <= 232448, "backward shared memory exceeds the 227 KB per-CTA limit");
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -527,7 +527,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (stages & kBwdFinalize) {
     const long long n_vec4 = (long long)a.B * a.Hq * a.N * D / 4;
     const long long want = (n_vec4 + 255) / 256;
     const unsigned blocks = (unsigned)(want < 152 * 32 ? want : 152 * 32);
@@ -535,11 +535,12 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a) {
                                                       n_vec4, a.scale);
     return cudaGetLastError();
   }
+  return cudaSuccess;
 }
 
-cudaError_t launch_bwd(const BwdLaunch& a) {
-  if (a.d == 128) return launch_bwd_t<128>(a);
-  return launch_bwd_t<64>(a);
+cudaError_t launch_bwd(const BwdLaunch& a, int stages) {
+  if (a.d == 128) return launch_bwd_t<128>(a, stages);
+  return launch_bwd_t<64>(a, stages);
 }
 
 }  // namespace fa

@@ -42,7 +42,10 @@ struct BwdLaunch {
   float scale;
   cudaStream_t stream;
 };
-cudaError_t launch_bwd(const BwdLaunch& a);
+// Backward stages (bit mask): 1 = prepare (delta, LSE2, zero dQ accumulator), 2 = compute
+// (main kernel: dK, dV, dQ accumulation), 4 = finalize (dQ accumulator -> bf16 dq).
+enum : int { kBwdPrepare = 1, kBwdCompute = 2, kBwdFinalize = 4, kBwdAll = 7 };
+cudaError_t launch_bwd(const BwdLaunch& a, int stages);
 
 inline int round_up_tile(int n) { return (n + kTile - 1) / kTile * kTile; }
 

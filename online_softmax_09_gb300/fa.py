@@ -46,6 +46,12 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd.restype = _i
+        L.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _vp]
+        L.fa_bwd_prepare.restype = _i
+        L.fa_bwd_compute.argtypes = [_vp] * 7 + [ctypes.c_size_t, _i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_bwd_compute.restype = _i
+        L.fa_bwd_finalize.argtypes = [_vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_bwd_finalize.restype = _i
         L.fa_check.argtypes = [_vp]
         L.fa_check.restype = _i
         L.fa_strerror.argtypes = [_i]
@@ -116,6 +122,33 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
                      B, Hq, Hkv, N, d, int(bool(causal)), sc, _stream_handle(stream, q.device))
     if r != FA_OK:
         raise FAError(r, "fa_bwd")
+    return dq, dk, dv
+
+
+def backward_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, causal: bool = False,
+                    scale: float | None = None, stream=None, between=None):
+    """Run fa_bwd_prepare, fa_bwd_compute and fa_bwd_finalize; ``between(i)`` (optional)
+    is called before stage i (0, 1, 2) and after the last (3), e.g. to record CUDA events."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    sc = 0.0 if scale is None else float(scale)
+    h = _stream_handle(stream, q.device)
+    nb = workspace.numel() * workspace.element_size()
+    L = lib()
+    calls = (
+        lambda: L.fa_bwd_prepare(o.data_ptr(), do.data_ptr(), lse.data_ptr(), workspace.data_ptr(), nb,
+                                 B, Hq, Hkv, N, d, h),
+        lambda: L.fa_bwd_compute(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), workspace.data_ptr(), nb, B, Hq, Hkv, N, d, int(bool(causal)), sc, h),
+        lambda: L.fa_bwd_finalize(dq.data_ptr(), workspace.data_ptr(), nb, B, Hq, Hkv, N, d, sc, h),
+    )
+    for i, call in enumerate(calls):
+        if between is not None:
+            between(i)
+        r = call()
+        if r != FA_OK:
+            raise FAError(r, ("fa_bwd_prepare", "fa_bwd_compute", "fa_bwd_finalize")[i])
+    if between is not None:
+        between(3)
     return dq, dk, dv
 
 

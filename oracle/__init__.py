@@ -34,6 +34,7 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_forward_head,
     attention_probs,
+    attention_query_block,
     attention_rows,
     brute_force_attention,
     causal_tile_counts,

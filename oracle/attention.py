@@ -409,3 +409,35 @@ def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: fl
         dV += Pt.T @ do[rows]
         dK += scale * (dSt.T @ q[rows])
     return dQ, dK, dV
+
+
+def attention_query_block(q, k, v, do, rows, causal: bool, scale: float):
+    """Forward and backward share of ONE block of query rows of one head.
+
+    Standard attention is row-separable in the queries: O, LSE and dQ of a query row
+    depend only on that row, and dK, dV are sums over query rows of per-row terms
+    (``dV = sum_i P_i^T dO_i``, ``dK = scale sum_i dS_i^T Q_i``). This returns, for the
+    rows ``rows``: ``O_R``, ``LSE_R``, ``dQ_R`` and the rows' contributions ``dK_R``,
+    ``dV_R`` (full N x d arrays), with the same definitions as
+    :func:`attention_forward_head` and :func:`attention_backward_head`. Summing the
+    contributions over a partition of the rows gives the full dK and dV.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    rows = np.asarray(rows)
+    S = scale * (q[rows] @ k.T)
+    if causal:
+        S = np.where(np.arange(k.shape[0])[None, :] > rows[:, None], -np.inf, S)
+    m = S.max(axis=1, keepdims=True)
+    P = np.exp(S - m)
+    l = P.sum(axis=1, keepdims=True)
+    P = P / l
+    O = P @ v
+    delta = np.sum(do[rows] * O, axis=1, keepdims=True)
+    dS = P * (do[rows] @ v.T - delta)
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q[rows])
+    dV = P.T @ do[rows]
+    return O, m[:, 0] + np.log(l[:, 0]), dQ, dK, dV

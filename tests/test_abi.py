@@ -27,7 +27,8 @@ def _declared():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_stats", "fa_check", "fa_strerror", "fa_version"):
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_fwd_stats", "fa_check", "fa_strerror", "fa_version",
+              "fa_bwd_prepare", "fa_bwd_compute", "fa_bwd_finalize"):
         assert n in names
 
 

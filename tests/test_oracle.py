@@ -324,3 +324,22 @@ def test_backward_rows_matches_full_backward(causal):
     np.testing.assert_allclose(rq, dq[qr], atol=1e-12)
     np.testing.assert_allclose(rk, dk[kr], atol=1e-12)
     np.testing.assert_allclose(rv, dv[kr], atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_query_blocks_sum_to_full_backward(causal):
+    rng = _rng(25)
+    N, d = 50, 5
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    O, lse = oracle.attention_forward_head(q, k, v, causal, 0.3)
+    dq, dk, dv = oracle.attention_backward_head(q, k, v, do, causal, 0.3)
+    sk, sv = np.zeros_like(dk), np.zeros_like(dv)
+    for blk in (np.arange(0, 17), np.arange(17, 40), np.arange(40, 50)):
+        Ob, lb, qb, kb, vb = oracle.attention_query_block(q, k, v, do, blk, causal, 0.3)
+        np.testing.assert_allclose(Ob, O[blk], atol=1e-13)
+        np.testing.assert_allclose(lb, lse[blk], atol=1e-13)
+        np.testing.assert_allclose(qb, dq[blk], atol=1e-12)
+        sk += kb
+        sv += vb
+    np.testing.assert_allclose(sk, dk, atol=1e-12)
+    np.testing.assert_allclose(sv, dv, atol=1e-12)
