@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Attention throughput on GB300: TFLOP/s of forward and of forward+backward (bf16, causal).
+
+One step = one pass of the whole path on one batch: fa_fwd (O, LSE) then the three backward
+stages (fa_bwd_prepare, fa_bwd_compute, fa_bwd_finalize) on the Llama-3.1-8B-shaped causal
+workload B=4, Hq=32, Hkv=8 (GQA 4:1), N=4096, d=128, bf16, inputs N(0,1)*0.5 from seed 2.
+FLOPs are algorithmic: 4*d per visible (query, key) pair for the forward (2*d*N*(N+1) per
+head, causal), 2.5x that for the backward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (launched by torch.distributed.run) every rank
+runs the same per-GPU workload on its own GPU with no data-path collective (weak scaling);
+the timing uses a barrier and the max over ranks. `--impl reference` times the fp64 CPU
+oracle on the host cores on bounded samples of the same workload.
+`--batch B` shrinks the batch for profiling runs only; such a line is not a bench value.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd (bf16, d=128, causal) and % of dense BF16 peak"
+WL = dict(B=4, Hq=32, Hkv=8, N=4096, d=128, causal=True, value_scale=0.5, seed=2)
+WORKLOAD_NAME = "llama3.1-8b attention: B=4 Hq=32 Hkv=8 N=4096 d=128 causal bf16, fwd+bwd"
+BWD_FACTOR = 2.5
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_bwd_compute_llama8b_traffic.txt")
+KERNEL_SOURCES = ["online_softmax_09_gb300/csrc/fa_bwd.cu", "online_softmax_09_gb300/csrc/fa_ptx.cuh"]
+
+
+def fwd_flops(B, Hq, N, d, causal):
+    pairs = N * (N + 1) // 2 if causal else N * N
+    return 4 * d * pairs * B * Hq
+
+
+def rows_flops(rows, d, causal, N):
+    """fwd+bwd algorithmic FLOPs of a block of query rows of one head."""
+    pairs = sum((i + 1) if causal else N for i in rows)
+    return 4 * d * pairs * (1 + BWD_FACTOR)
+
+
+def config_block():
+    return {"workload": WORKLOAD_NAME, "B": WL["B"], "Hq": WL["Hq"], "Hkv": WL["Hkv"], "N": WL["N"], "d": WL["d"],
+            "causal": WL["causal"], "inputs": "iid N(0,1)*0.5 from seed 2, cast to bf16",
+            "l2": "inputs larger than L2: ~0.9 GB touched per step (q,k,v,o,dO,dq,dk,dv,workspace), no flush",
+            "parallelism": "replicas (independent per-GPU workload, no collective)"}
+
+
+def cores_used():
+    n = len(os.sched_getaffinity(0))
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return min(n, int(os.environ[var]))
+    return n
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the backward compute kernel from the committed ncu summary,
+    or None when that summary was taken on different kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.loads(f.read().split("\n---\n", 1)[0])
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------------------------
+# Clock sampling (nvidia-smi) during the timed region.
+# --------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------------------------
+# Our arm: the CUDA path through the C ABI.
+# --------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B = args.batch if args.batch else WL["B"]
+    Hq, Hkv, N, d, causal = WL["Hq"], WL["Hkv"], WL["N"], WL["d"], WL["causal"]
+
+    qh, kh, vh, doh = make_qkv(B, Hq, Hkv, N, d, seed=WL["seed"], value_scale=WL["value_scale"], with_do=True)
+    q, k, v, do = (t.to(dev) for t in (qh, kh, vh, doh))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    f_fwd = fwd_flops(B, Hq, N, d, causal)
+    f_step = f_fwd * (1 + BWD_FACTOR)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.forward(q, k, v, causal, out=o, lse=lse)
+        fa.backward_stages(q, k, v, o, do, lse, dq, dk, dv, ws, causal,
+                           between=(lambda i: ev[i + 1].record(stream)) if ev is not None else None)
+
+    for _ in range(args.warmup):
+        step()
+    fa.check()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clock = ClockSampler("GPU-" + str(torch.cuda.get_device_properties(dev).uuid)) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clock:
+        clock.start()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = clock.stop() if clock else None
+    fa.check()
+    total_ms = t0.elapsed_time(t1)
+    # evs[i]: 0 before fa_fwd, 1 before prepare, 2 before compute, 3 before finalize, 4 after it
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_compute_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    e2e = None
+    if not args.no_e2e:
+        # End to end through the public API with host buffers: pinned host -> device copies of
+        # q, k, v, dO, the whole path, and device -> pinned host copies of o, lse, dq, dk, dv.
+        hin = [t.pin_memory() for t in (qh, kh, vh, doh)]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+        E = max(3, min(K, 50))
+
+        def e2e_step():
+            for h, dd in zip(hin, (q, k, v, do)):
+                dd.copy_(h, non_blocking=True)
+            fa.forward(q, k, v, causal, out=o, lse=lse)
+            fa.backward(q, k, v, o, do, lse, causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+            for h, dd in zip(hout, (o, lse, dq, dk, dv)):
+                h.copy_(dd, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        a0.record(stream)
+        for _ in range(E):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        fa.check()
+        e2e_ms = a0.elapsed_time(a1) / E
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(world * f_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4),
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    burst, sustained, src = load_peaks()
+    ms_step = total_ms / K
+    value = world * f_step / (ms_step * 1e-3) / 1e12
+    achieved = f_fwd * BWD_FACTOR / (bwd_compute_ms * 1e-3) / 1e12
+    cfg = config_block()
+    if B != WL["B"]:
+        cfg["workload"] = f"PROFILING CASE (not a bench value): batch {B} instead of {WL['B']}"
+        cfg["B"] = B
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": cfg,
+        "fwd": {"tflops": round(f_fwd / (fwd_ms * 1e-3) / 1e12, 2), "ms": round(fwd_ms, 4),
+                "pct_of_peak_burst": round(100 * f_fwd / (fwd_ms * 1e-3) / 1e12 / burst, 2)},
+        "fwd_bwd": {"tflops": round(value / world, 2), "ms": round(fwd_ms + bwd_ms, 4),
+                    "pct_of_peak_sustained": round(100 * value / world / sustained, 2)},
+        "roofline": {"kernel": "fa_bwd_main_kernel<128> (fa_bwd_compute)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": sustained, "unit": "TFLOP/s",
+                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+                     "frac": round(achieved / sustained, 4), "traffic": measured_traffic(),
+                     "algorithmic_flops_per_launch": f_fwd * BWD_FACTOR, "ms_per_launch": round(bwd_compute_ms, 4)},
+        "e2e": e2e,
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(qh, kh, vh, doh, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------------------------
+# The fp64 CPU oracle on the host cores (reported baseline; never the product path).
+# --------------------------------------------------------------------------------------------
+def _oracle_blocks(qh, kh, vh, doh, rows_per_block):
+    """Endless sequence of (head arrays, rows) samples of the workload: blocks of query rows
+    of one head at a time, walking the rows from the end (the longest causal rows first)."""
+    from online_softmax_09_gb300.inputs import to_f64
+
+    G = WL["Hq"] // WL["Hkv"]
+    N = qh.shape[2]
+    heads = [(b, h) for b in range(qh.shape[0]) for h in range(qh.shape[1])]
+    cache = {}
+    while True:
+        for b, h in heads:
+            if (b, h) not in cache:
+                cache.clear()
+                cache[(b, h)] = tuple(to_f64(t) for t in (qh[b, h], kh[b, h // G], vh[b, h // G], doh[b, h]))
+            for end in range(N, 0, -rows_per_block):
+                yield cache[(b, h)], list(range(max(0, end - rows_per_block), end))
+
+
+def cpu_baseline(qh, kh, vh, doh, budget_s=15.0, rows_per_block=256):
+    import oracle
+
+    scale = 1 / math.sqrt(WL["d"])
+    done_flops, done_rows, t_used = 0.0, 0, 0.0
+    for arrs, rows in _oracle_blocks(qh, kh, vh, doh, rows_per_block):
+        t = time.perf_counter()
+        oracle.attention_query_block(*arrs, rows, WL["causal"], scale)
+        t_used += time.perf_counter() - t
+        done_flops += rows_flops(rows, WL["d"], WL["causal"], WL["N"])
+        done_rows += len(rows)
+        if t_used >= budget_s:
+            break
+    return {"value": round(done_flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": cores_used(),
+            "kind": "oracle",
+            "sample": f"fp64 NumPy oracle (S and P materialised), fwd+bwd of {done_rows} query rows starting at "
+                      f"head (0,0), {rows_per_block}-row blocks from the last row down, {t_used:.1f} s of host time"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    qh, kh, vh, doh = make_qkv(WL["B"], WL["Hq"], WL["Hkv"], WL["N"], WL["d"], seed=WL["seed"],
+                               value_scale=WL["value_scale"], with_do=True)
+    scale = 1 / math.sqrt(WL["d"])
+    # Size each step so that warm-up + timed steps take about two minutes of host time.
+    budget = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    gen = _oracle_blocks(qh, kh, vh, doh, 64)
+    arrs, rows = next(gen)
+    t = time.perf_counter()
+    oracle.attention_query_block(*arrs, rows, WL["causal"], scale)
+    per_row = (time.perf_counter() - t) / len(rows)
+    rpb = int(max(8, min(WL["N"], budget / max(per_row, 1e-9))))
+    gen = _oracle_blocks(qh, kh, vh, doh, rpb)
+    for _ in range(args.warmup):
+        arrs, rows = next(gen)
+        oracle.attention_query_block(*arrs, rows, WL["causal"], scale)
+    flops, secs, nrows = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        arrs, rows = next(gen)
+        t = time.perf_counter()
+        oracle.attention_query_block(*arrs, rows, WL["causal"], scale)
+        secs += time.perf_counter() - t
+        flops += rows_flops(rows, WL["d"], WL["causal"], WL["N"])
+        nrows += len(rows)
+    value = flops / secs / 1e12
+    sample = (f"fp64 NumPy oracle, fwd+bwd of up to {rpb} query rows per step ({nrows} rows in total) of the same "
+              f"workload, rows walked from the last row of head (0,0) down")
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_block(),
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
