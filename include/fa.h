@@ -125,6 +125,30 @@ int fa_bwd_finalize(void *dq, void *workspace, size_t workspace_bytes,
                     int B, int Hq, int Hkv, int N, int d, float scale, fa_stream_t stream);
 
 /*
+ * Backward pass for callers that cannot allocate device memory. The pages this library
+ * follows have no counterpart to this entry point; it exists for callers that must not call
+ * cudaMalloc, such as a plugin inside a host runtime that owns and budgets all device memory,
+ * or a latency-critical loop where cudaMalloc's implicit device synchronisation is not
+ * allowed. It computes exactly what fa_bwd computes (same arguments, minus the workspace) and
+ * takes the workspace from a fixed device array of FA_BWD_NOALLOC_MAX_BYTES bytes inside the
+ * library, which every GPU that loads the library holds until the process exits.
+ *   - Returns FA_ERR_WORKSPACE, launching nothing, when fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
+ *     exceeds FA_BWD_NOALLOC_MAX_BYTES (64 MiB: e.g. B*Hq*N up to about 129,000 query rows
+ *     at d = 128, or 254,000 at d = 64; rows are counted after rounding N up to a multiple of 128).
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - All calls on a device share the one array. Calls whose kernels overlap on the GPU (on
+ *     different streams, or from different threads) race on it and give wrong results;
+ *     serialise them. Calls in sequence are safe: each call clears what must start at zero.
+ *   - Nothing is allocated or freed.
+ */
+#define FA_BWD_NOALLOC_MAX_BYTES ((size_t)64 << 20)
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                   const float *lse, void *dq, void *dk, void *dv,
+                   int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                   fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting) or FA_ERR_LAUNCH (the stream reported
  * a CUDA error).
