@@ -1,22 +1,28 @@
 // fa_fwd.cu -- forward pass of exact softmax attention on sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, query head):
-//   warp 4      TMA producer: Q once, then K_j / V_j tiles into an NS-stage ring.
-//   warp 5      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T (smem x smem -> TMEM),
-//               O += P_j V_j (P from TMEM, V from smem -> TMEM).
-//   warps 0-3   softmax warpgroup, one thread per query row: running max m and sum l
-//               ("FlashAttention Implementation > How FlashAttention Uses Tiling", "The Running
-//               Statistics"), correction exp(m_old - m_new) applied to l and to the output
-//               accumulator in TMEM ("Why the Correction Factor Works"), P = exp(S - m) written
-//               back to TMEM as bf16, and the epilogue O = acc / l, LSE = m + ln l
-//               ("LLM Architecture Refresh [3]", section 4).
-// Causal: key tiles after the query tile are never loaded or computed (same post, section
-// 7); the diagonal tile and a ragged last tile are masked element-wise.
+// One CTA computes two 128-row query tiles (256 consecutive rows) of one (batch, query head);
+// both tiles share every K/V tile loaded:
+//   warp 8      TMA producer: Q0, Q1 once, then K_j into an NK-stage ring and V_j into an
+//               NV-stage ring.
+//   warp 9      MMA issuer (one thread) and TMEM owner. Issue order per key tile j:
+//                 O0 += P0_j V_j, S0_{j+1} = Q0 K_{j+1}^T, O1 += P1_j V_j, S1_{j+1} = Q1 K_{j+1}^T
+//               so that while one softmax warpgroup turns S into P, the tensor core works on
+//               the other tile.
+//   warps 0-3   softmax warpgroup of tile 0, warps 4-7 of tile 1: one thread per query row,
+//               running max m and sum l ("FlashAttention Implementation > How FlashAttention
+//               Uses Tiling", "The Running Statistics"), correction exp(m_old - m_new) applied
+//               to l and to the output accumulator in TMEM ("Why the Correction Factor
+//               Works"), P = exp(S - m) written back to TMEM as bf16 over the S columns, and
+//               the epilogue O = acc / l, LSE = m + ln l ("LLM Architecture Refresh [3]",
+//               section 4).
+// Causal: key tiles after a query tile are never loaded or computed (same post, section 7);
+// the diagonal tile and a ragged last tile are masked element-wise.
 //
-// TMEM columns: S/P double buffer at [0,128) and [128,256); O accumulator at [256, 256+D).
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // The running max is kept in base-2 units (scores scaled by scale*log2 e) so P uses the
 // hardware exp2. The max is the true running max: l and O are rescaled whenever a tile raises
 // it, so the largest weight of each row is exactly 1 and loses nothing to bf16 rounding.
+// S is read from TMEM twice (once for the row max, once for P) to keep registers low.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -29,25 +35,27 @@ struct FwdParams {
   uint32_t* status;
   int B, Hq, Hkv, N, causal;
   int num_tiles;     // ceil(N / 128): query tiles per head == key tiles per head
+  int num_pairs;     // ceil(num_tiles / 2): CTAs per head
   float scale_log2;  // scale * log2(e)
 };
 
-template <int D, int NS>
+template <int D, int NK, int NV>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + NS * kTileBytes;
-  static constexpr int kBar = kV + NS * kTileBytes;
+  static constexpr int kQ = 0;  // Q0, Q1
+  static constexpr int kK = kQ + 2 * kTileBytes;
+  static constexpr int kV = kK + NK * kTileBytes;
+  static constexpr int kBar = kV + NV * kTileBytes;
   // mbarrier indices
-  static constexpr int bQ = 0;
-  static constexpr int bKFull = 1;
-  static constexpr int bVFull = bKFull + NS;
-  static constexpr int bKVEmpty = bVFull + NS;
-  static constexpr int bSFull = bKVEmpty + NS;  // 2
-  static constexpr int bPFull = bSFull + 2;     // 2
-  static constexpr int bOFull = bPFull + 2;
-  static constexpr int bDrain = bOFull + 1;
+  static constexpr int bQ = 0;                // 2
+  static constexpr int bKFull = bQ + 2;       // NK
+  static constexpr int bKEmpty = bKFull + NK; // NK
+  static constexpr int bVFull = bKEmpty + NK; // NV
+  static constexpr int bVEmpty = bVFull + NV; // NV
+  static constexpr int bSFull = bVEmpty + NV; // 2 (per tile)
+  static constexpr int bPFull = bSFull + 2;   // 2
+  static constexpr int bOFull = bPFull + 2;   // 2
+  static constexpr int bDrain = bOFull + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -55,14 +63,31 @@ struct FwdSmem {
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
 };
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kNegInf = 0xff800000u;
 
-template <int D, int NS>
+__device__ __forceinline__ float max32(const uint32_t (&s)[32]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], fmaxf(__uint_as_float(s[i + 16]), __uint_as_float(s[i + 24])));
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+// Columns past `lim` (the last visible key of this row within the tile) become -inf.
+__device__ __forceinline__ void mask32(uint32_t (&s)[32], int col0, int lim) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (col0 + i > lim) s[i] = kNegInf;
+}
+
+template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdSmem<D, NS>;
+  using L = FwdSmem<D, NK, NV>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -78,38 +103,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item. Causal tiles are issued longest first: blockIdx 0.. take the last query tile.
+  // Work item: query tiles 2*pair and 2*pair+1 of head bh. Causal pairs run longest first.
   const int BH = p.B * p.Hq;
   const int rank = blockIdx.x / BH;
   const int bh = blockIdx.x - rank * BH;
-  const int q_tile = p.causal ? (p.num_tiles - 1 - rank) : rank;
+  const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
   const int b = bh / p.Hq;
   const int hq = bh - b * p.Hq;
   const int kv_z = b * p.Hkv + hq / (p.Hq / p.Hkv);
-  const int q0 = q_tile * kTile;
-  const int n_kv = p.causal ? (q_tile + 1) : p.num_tiles;
+  const int qt0 = 2 * pair;
+  const bool has1 = qt0 + 1 < p.num_tiles;
+  // Key tiles each query tile visits.
+  const int n0 = p.causal ? (qt0 + 1) : p.num_tiles;
+  const int n1 = has1 ? (p.causal ? (qt0 + 2) : p.num_tiles) : 0;
+  const int n_max = has1 ? n1 : n0;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::bQ), 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::bQ + t), 1);
+      mbar_init(bar(L::bSFull + t), 1);
+      mbar_init(bar(L::bPFull + t), 128);
+      mbar_init(bar(L::bOFull + t), 1);
+    }
+    for (int s = 0; s < NK; ++s) {
       mbar_init(bar(L::bKFull + s), 1);
+      mbar_init(bar(L::bKEmpty + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(bar(L::bVFull + s), 1);
-      mbar_init(bar(L::bKVEmpty + s), 1);
+      mbar_init(bar(L::bVEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(L::bSFull + i), 1);
-      mbar_init(bar(L::bPFull + i), 128);
-    }
-    mbar_init(bar(L::bOFull), 1);
     mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -118,80 +150,102 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       constexpr uint32_t kBytes = L::kTileBytes;
-      mbar_expect_tx(bar(L::bQ), kBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * 16384, &tm_q, bar(L::bQ), c * 64, q0, bh);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NS;
-        if (!mbar_wait(bar(L::bKVEmpty + s), ((j / NS) & 1) ^ 1, ctl)) break;
-        const uint32_t k_dst = sK + s * L::kTileBytes;
-        const uint32_t v_dst = sV + s * L::kTileBytes;
-        mbar_expect_tx(bar(L::bKFull + s), kBytes);
+      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+        mbar_expect_tx(bar(L::bQ + t), kBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(k_dst + c * 16384, &tm_k, bar(L::bKFull + s), c * 64, j * kTile, kv_z);
-        mbar_expect_tx(bar(L::bVFull + s), kBytes);
+          tma_load_3d(sQ + t * kBytes + c * 16384, &tm_q, bar(L::bQ + t), c * 64, (qt0 + t) * kTile, bh);
+      }
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n_max; ++j) {
+        const int sk = j % NK, sv = j % NV;
+        if (!mbar_wait(bar(L::bKEmpty + sk), ((j / NK) & 1) ^ 1, ctl)) break;
+        mbar_expect_tx(bar(L::bKFull + sk), kBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(v_dst + c * 16384, &tm_v, bar(L::bVFull + s), c * 64, j * kTile, kv_z);
-        issued = j + 1;
+          tma_load_3d(sK + sk * kBytes + c * 16384, &tm_k, bar(L::bKFull + sk), c * 64, j * kTile, kv_z);
+        k_issued = j + 1;
+        if (!mbar_wait(bar(L::bVEmpty + sv), ((j / NV) & 1) ^ 1, ctl)) break;
+        mbar_expect_tx(bar(L::bVFull + sv), kBytes);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sV + sv * kBytes + c * 16384, &tm_v, bar(L::bVFull + sv), c * 64, j * kTile, kv_z);
+        v_issued = j + 1;
       }
       if (*abort_flag) {  // let every copy still in flight land before shared memory is freed
         drain_wait(bar(L::bQ), 0);
-        for (int j = issued > NS ? issued - NS : 0; j < issued; ++j) {
-          drain_wait(bar(L::bKFull + j % NS), (j / NS) & 1);
-          drain_wait(bar(L::bVFull + j % NS), (j / NS) & 1);
-        }
+        if (has1) drain_wait(bar(L::bQ + 1), 0);
+        for (int j = k_issued > NK ? k_issued - NK : 0; j < k_issued; ++j)
+          drain_wait(bar(L::bKFull + j % NK), (j / NK) & 1);
+        for (int j = v_issued > NV ? v_issued - NV : 0; j < v_issued; ++j)
+          drain_wait(bar(L::bVFull + j % NV), (j / NV) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      auto issue_s = [&](int t) -> bool {
-        const int s = t % NS;
-        if (!mbar_wait(bar(L::bKFull + s), (t / NS) & 1, ctl)) return false;
+      auto issue_s = [&](int t, int j) -> bool {
+        const int sk = j % NK;
+        if (!mbar_wait(bar(L::bKFull + sk), (j / NK) & 1, ctl)) return false;
         tc_fence_after();
-        const uint32_t k_base = sK + s * L::kTileBytes;
+        const uint32_t q_base = sQ + t * L::kTileBytes;
+        const uint32_t k_base = sK + sk * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major, 128B swizzle: 64-element column blocks 16 KB apart, 16 elements = 32 B.
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS[t & 1], sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024),
-                 idS, kk > 0);
+          mma_ss(tmem + 128 * t, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idS,
+                 kk > 0);
         }
-        mma_commit(bar(L::bSFull + (t & 1)));
+        mma_commit(bar(L::bSFull + t));
+        return true;
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int sv = j % NV;
+        if (!mbar_wait(bar(L::bPFull + t), j & 1, ctl)) return false;
+        if (!mbar_wait(bar(L::bVFull + sv), (j / NV) & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t v_base = sV + sv * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          // V as the MN-major B operand: 16 keys = 2 swizzle atoms of 8 rows x 128 B.
+          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024),
+                 idO, (j > 0 || kk > 0));
+        }
+        mma_commit(bar(L::bOFull + t));
         return true;
       };
       bool ok = mbar_wait(bar(L::bQ), 0, ctl);
       if (ok) {
         tc_fence_after();
-        ok = issue_s(0);
+        ok = issue_s(0, 0);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) break;
-        const int s = j % NS;
-        if (!mbar_wait(bar(L::bPFull + (j & 1)), (j >> 1) & 1, ctl)) break;
-        if (!mbar_wait(bar(L::bVFull + s), (j / NS) & 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t v_base = sV + s * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // V as the MN-major B operand: 16 keys = 2 swizzle atoms of 8 rows x 128 B.
-          mma_ts(tO, tS[j & 1] + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024), idO,
-                 (j > 0 || kk > 0));
+      if (ok && has1) {
+        ok = mbar_wait(bar(L::bQ + 1), 0, ctl);
+        if (ok) {
+          tc_fence_after();
+          ok = issue_s(1, 0);
         }
-        mma_commit(bar(L::bKVEmpty + s));
-        mma_commit(bar(L::bOFull));
+      }
+      if (ok) mma_commit(bar(L::bKEmpty));  // K_0 released once both score MMAs complete
+      for (int j = 0; ok && j < n_max; ++j) {
+        if (j < n0) {
+          if (!(ok = issue_pv(0, j))) break;
+          if (j + 1 < n0 && !(ok = issue_s(0, j + 1))) break;
+        }
+        if (j < n1) {
+          if (!(ok = issue_pv(1, j))) break;
+          if (j + 1 < n1 && !(ok = issue_s(1, j + 1))) break;
+        }
+        mma_commit(bar(L::bVEmpty + j % NV));
+        if (j + 1 < n_max) mma_commit(bar(L::bKEmpty + (j + 1) % NK));
       }
       if (*abort_flag) {  // wait for issued MMAs before tensor memory is released
         mma_commit(bar(L::bDrain));
@@ -199,65 +253,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int row = q0 + threadIdx.x;
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;  // query tile of this warpgroup
+    const int n_kv = t ? n1 : n0;
+    const int qt = qt0 + t;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 128 * t + lane_off;
+    const uint32_t tO = tmem + 256 + 128 * t + lane_off;
+    const int row = qt * kTile + (threadIdx.x & 127);
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
     uint32_t n_rescaled = 0;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_warp(bar(L::bSFull + sb), (j >> 1) & 1, ctl)) {
+      if (!mbar_wait_warp(bar(L::bSFull + t), j & 1, ctl)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t t_row = tS[sb] + lane_off;
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_row + c * 32, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
       const int kv0 = j * kTile;
-      if ((p.causal && j == q_tile) || kv0 + kTile > p.N) {
-        const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;  // last visible column
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i > lim) sr[c][i] = 0xff800000u;  // -inf
-      }
+      const bool need_mask = (p.causal && j == qt) || kv0 + kTile > p.N;
+      const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;  // last visible column
+      // Pass 1: row max.
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t a[32], b2[32];
+        tmem_ld32(tS + c * 32, a);
+        tmem_ld32(tS + (c + 1) * 32, b2);
+        tmem_ld_wait(a);
+        tmem_ld_wait(b2);
+        if (need_mask) {
+          mask32(a, c * 32, lim);
+          mask32(b2, (c + 1) * 32, lim);
+        }
+        mx = fmaxf(mx, fmaxf(max32(a), max32(b2)));
+      }
       // Running max in base-2 units; correction exp(m_old - m_new) (0 on the first tile).
       const float m_new = fmaxf(m_run, mx * sl2);
       const float corr = (m_new > m_run) ? ex2(m_run - m_new) : 1.f;
       if (j > 0 && m_new > m_run && row < p.N) ++n_rescaled;
       m_run = m_new;
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float sum = 0.f;
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][i]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][i + 1]), sl2, -m_use));
-          sum += p0 + p1;
-          pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
-        }
-      l_run = l_run * corr + sum;
-      tmem_st32(t_row, pk[0]);
-      tmem_st32(t_row + 32, pk[1]);
       if (j > 0) {
-        // Wait for O += P_{j-1} V_{j-1}. Waiting at every tile keeps this warp's view of the
-        // barrier's phase exact; the wait overlaps the tail of that MMA only.
-        if (!mbar_wait_warp(bar(L::bOFull), (j - 1) & 1, ctl)) {
+        // O += P_{j-1} V_{j-1} has completed before S_j did; this wait at every tile keeps the
+        // warp's view of the barrier phase exact and returns at once.
+        if (!mbar_wait_warp(bar(L::bOFull + t), (j - 1) & 1, ctl)) {
           ok = false;
           break;
         }
@@ -266,28 +308,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_ld32(tO + c * 32, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-            tmem_st32(tO + lane_off + c * 32, o);
+            tmem_st32(tO + c * 32, o);
           }
         }
       }
+      // Pass 2: P = 2^(S*scale*log2e - m) as bf16 over the S columns already read, and row sum.
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tS + c * 32, a);
+        tmem_ld_wait(a);
+        if (need_mask) mask32(a, c * 32, lim);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(a[i]), sl2, -m_use));
+          const float p1 = ex2(fmaf(__uint_as_float(a[i + 1]), sl2, -m_use));
+          sum[(i >> 1) & 3] += p0 + p1;
+          pk[i >> 1] = pack_bf16(p0, p1);
+        }
+        // P chunk c covers columns [16c, 16c+16): S columns that pass 2 has already read.
+        tmem_st16(tS + c * 16, pk);
+      }
+      l_run = l_run * corr + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::bPFull + sb));
+      mbar_arrive(bar(L::bPFull + t));
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok) ok = mbar_wait_warp(bar(L::bOFull), (n_kv - 1) & 1, ctl);
-    if (ok) {
+    if (ok && n_kv > 0) ok = mbar_wait_warp(bar(L::bOFull + t), (n_kv - 1) & 1, ctl);
+    if (ok && n_kv > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const size_t row_off = ((size_t)bh * p.N + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_ld_wait(o);
         uint4 w[4];
         uint32_t* wp = reinterpret_cast<uint32_t*>(w);
@@ -302,12 +364,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
     }
-    if (p.counters != nullptr) {
+    if (p.counters != nullptr && n_kv > 0) {
       unsigned int r = n_rescaled;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
       if (lane == 0 && r) atomicAdd(&p.counters[2], (unsigned long long)r);
-      if (threadIdx.x == 0) {
+      if ((threadIdx.x & 127) == 0) {
         atomicAdd(&p.counters[0], (unsigned long long)n_kv);
         atomicAdd(&p.counters[1], (unsigned long long)(p.num_tiles - n_kv));
       }
@@ -317,20 +379,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // ------------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-template <int D, int NS>
+template <int D, int NK, int NV>
 static cudaError_t launch_fwd_t(const FwdLaunch& a, const FwdParams& p) {
-  constexpr int smem = FwdSmem<D, NS>::kAlloc;
+  constexpr int smem = FwdSmem<D, NK, NV>::kAlloc;
   static_assert(smem <= 232448, "forward shared memory exceeds the 227 KB per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(fa_fwd_kernel<D, NK, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.num_tiles * p.B * p.Hq;
-  fa_fwd_kernel<D, NS><<<(unsigned)grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+  const long long grid = (long long)p.num_pairs * p.B * p.Hq;
+  fa_fwd_kernel<D, NK, NV><<<(unsigned)grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
   return cudaGetLastError();
 }
 
@@ -346,9 +409,10 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.N = a.N;
   p.causal = a.causal;
   p.num_tiles = (a.N + kTile - 1) / kTile;
+  p.num_pairs = (p.num_tiles + 1) / 2;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (a.d == 128) return launch_fwd_t<128, 2>(a, p);
-  return launch_fwd_t<64, 4>(a, p);
+  if (a.d == 128) return launch_fwd_t<128, 3, 2>(a, p);
+  return launch_fwd_t<64, 4, 4>(a, p);
 }
 
 }  // namespace fa
