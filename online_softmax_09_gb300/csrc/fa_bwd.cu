@@ -12,21 +12,22 @@
 //      the fp32 dQ accumulator.                                               (HBM-bound)
 //   2. main: one CTA per (batch, kv head, 128-key tile). It keeps K_n and V_n in shared
 //      memory and the dK, dV accumulators in TMEM, and loops over the G query heads of its
-//      group and their query tiles (causal: from the diagonal tile on). Per query tile:
-//        MMA  dP^T = V_n dO_i^T   and   S^T = K_n Q_i^T          (smem x smem -> TMEM)
-//        softmax warps (thread = key row): P^T = 2^(S^T scale log2e - LSE2), bf16 -> TMEM
-//        MMA  dV += P^T dO_i                                     (TMEM x smem -> TMEM)
-//        softmax warps: dS^T = P^T (dP^T - delta), bf16 -> TMEM and -> shared memory
-//        MMA  dK += dS^T Q_i ;  dQ_i = dS K_n  (into the S^T columns, now free)
+//      group and their query tiles (causal: from the diagonal tile on). Per query tile i:
+//        softmax warps (thread = key row): P_i^T = 2^(S_i^T scale log2e - LSE2), bf16 -> TMEM
+//        MMA  dV += P_i^T dO_i ;  dP_i^T = V_n dO_i^T ;  S_{i+1}^T = K_n Q_{i+1}^T
+//        softmax warps: dS_i^T = P_i^T (dP_i^T - delta), bf16 -> TMEM and -> shared memory
+//        MMA  dK += dS_i^T Q_i ;  dQ_i = dS_i K_n  (into the dP^T columns, now free)
 //        drain warps (thread = query row): dQ_i TMEM -> fp32 red.global.add into the
 //        workspace accumulator.
+//      The next tile's S^T is computed while the softmax warps work on dS_i, and its P while
+//      the dK and dQ MMAs run, so the tensor core does not wait for the softmax warps.
 //   3. dQ conversion: dq = bf16(scale * accumulator).
 //
 // Warp roles of the main kernel: 0-3 softmax/dS and the final dK/dV epilogue, 4 TMA producer,
 // 5 MMA issuer and TMEM owner, 6-9 dQ drain.
-// TMEM columns: S^T/P^T/dQ [0,128), dP^T/dS^T [128,256), dV [256,256+D), dK [256+D,256+2D).
+// TMEM columns: S^T/P^T [0,128), dP^T/dS^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 // For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
-// after the dV MMA (the last reader of dO) has completed; for D = 64 it has its own buffer.
+// once the dV and dP MMAs (the readers of dO) have completed; for D = 64 it has its own buffer.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -138,7 +139,6 @@ struct BwdSmem {
     bDPFull,
     bPReady,
     bDSReady,
-    bDVDone,
     bSmemDS,
     bDQFull,
     bDQFree,
@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bDPFull), 1);
     mbar_init(bar(L::bPReady), 128);
     mbar_init(bar(L::bDSReady), 128);
-    mbar_init(bar(L::bDVDone), 1);
     mbar_init(bar(L::bSmemDS), 128);
     mbar_init(bar(L::bDQFull), 1);
     mbar_init(bar(L::bDQFree), 128);
@@ -228,8 +227,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;         // S^T, then P^T (bf16), then dQ
-  const uint32_t tdP = tmem + 128;  // dP^T, then dS^T (bf16)
+  const uint32_t tS = tmem;         // S^T, then P^T (bf16)
+  const uint32_t tdP = tmem + 128;  // dP^T, then dS^T (bf16), then dQ
   const uint32_t tdV = tmem + 256;
   const uint32_t tdK = tmem + 256 + D;
 
@@ -275,18 +274,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
+    // Per query tile i: dV += P_i^T dO_i, dP_i^T = V dO_i^T, S_{i+1}^T = K Q_{i+1}^T,
+    // dK += dS_i^T Q_i, dQ_i = dS_i K. The softmax warps compute dS_i while S_{i+1}^T runs and
+    // P_{i+1} while dK and dQ run; the dQ drain overlaps the next dV.
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
       constexpr uint32_t idDQ = idesc_bf16_f32(128, D, true, true);      // dQ
-      bool ok = mbar_wait(bar(L::bKV), 0, ctl);
+      auto issue_s = [&](int it) {  // S^T = K_n Q_it^T into tS
+        const uint32_t sQ = stage(it & 1) + L::kStQ;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
+        }
+        mma_commit(bar(L::bSFull));
+      };
+      bool ok = mbar_wait(bar(L::bKV), 0, ctl) && mbar_wait(bar(L::bQFull), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it & 1;
         const uint32_t ph = (it >> 1) & 1;
         const uint32_t sQ = stage(s) + L::kStQ;
         const uint32_t sDO = stage(s) + L::kStDO;
-        // dP^T = V_n dO_i^T
+        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand)
+        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
         if (!(ok = mbar_wait(bar(L::bDOFull + s), ph, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tdV, tS + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+        // dP^T = V_n dO_i^T, once the previous dQ has been drained out of these columns.
+        if (it > 0 && !(ok = mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -294,36 +316,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(bar(L::bDPFull));
-        // S^T = K_n Q_i^T, once the previous dQ has been drained out of these columns.
-        if (!(ok = mbar_wait(bar(L::bQFull + s), ph, ctl))) break;
-        if (it > 0 && !(ok = mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
+        // S^T of the next query tile (P_i^T in these columns was read by the dV MMA above).
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait(bar(L::bQFull + (s ^ 1)), ((it + 1) >> 1) & 1, ctl))) break;
+          tc_fence_after();
+          issue_s(it + 1);
         }
-        mma_commit(bar(L::bSFull));
-        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand)
-        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdV, tS + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
-        mma_commit(bar(L::bDVDone));
         // dK += dS^T Q_i
         if (!(ok = mbar_wait(bar(L::bDSReady), it & 1, ctl))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tdK, tdP + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
-        // dQ_i = dS K_n  (dS and K both MN-major in shared memory) into the S^T columns
+        // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns
         if (!(ok = mbar_wait(bar(L::bSmemDS), it & 1, ctl))) break;
         tc_fence_after();
         const uint32_t sds = sDS(s);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tS, sdesc_sw128(sds + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ,
+          mma_ss(tdP, sdesc_sw128(sds + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ,
                  kk > 0);
         mma_commit(bar(L::bDQFull));
         mma_commit(bar(L::bStageEmpty + s));
@@ -342,23 +353,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool key_ok = key < p.N;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
+    uint32_t pk[4][16];  // P_it^T as packed bf16, kept from the P phase to the dS phase
+    // P phase of query tile `it`: P^T = 2^(S^T scale log2e - LSE2), bf16 into TMEM and pk.
+    auto p_phase = [&](int it) -> bool {
       const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
       int hq, i;
       item(it, hq, i);
       const bool diag = p.causal && i == n;
       const float* sl = reinterpret_cast<const float*>(stage_ptr(s) + L::kStL);
-      const float* sd = reinterpret_cast<const float*>(stage_ptr(s) + L::kStD);
-      if (!(ok = mbar_wait_warp(bar(L::bQFull + s), ph, ctl))) break;
-      if (!(ok = mbar_wait_warp(bar(L::bSFull), it & 1, ctl))) break;
+      if (!mbar_wait_warp(bar(L::bQFull + s), (it >> 1) & 1, ctl)) return false;
+      if (!mbar_wait_warp(bar(L::bSFull), it & 1, ctl)) return false;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t sr[32];
         tmem_ld32(tS + lane_off + c * 32, sr);
         tmem_ld_wait(sr);
-        uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
@@ -370,59 +380,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pv[t] = ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
             if (!key_ok || (diag && q < kr)) pv[t] = 0.f;
           }
-          pk[j / 2] = pack_bf16(pv[0], pv[1]);
-          pk[j / 2 + 1] = pack_bf16(pv[2], pv[3]);
+          pk[c][j / 2] = pack_bf16(pv[0], pv[1]);
+          pk[c][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
         }
         // P^T (bf16) overwrites S^T columns [16c, 16c+16), all of which were read already.
-        tmem_st16(tS + lane_off + c * 16, pk);
+        tmem_st16(tS + lane_off + c * 16, pk[c]);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::bPReady));
-
-      if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), ph, ctl))) break;
+      return true;
+    };
+    ok = n_iter > 0 && p_phase(0);
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it & 1;
+      const float* sd = reinterpret_cast<const float*>(stage_ptr(s) + L::kStD);
+      if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), (it >> 1) & 1, ctl))) break;
       if (!(ok = mbar_wait_warp(bar(L::bDPFull), it & 1, ctl))) break;
       tc_fence_after();
-      // dS^T = P^T (dP^T - delta), with P^T read back as the bf16 values the dV MMA uses.
-      uint32_t dsp[4][16];
+      // dS^T = P^T (dP^T - delta) with the bf16 P the dV MMA used. dP_it^T being complete
+      // implies every earlier MMA is, so the dO slot (or the dS buffer) is free to overwrite.
+      const uint32_t row_base = sDS(s) + (uint32_t)kr * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t dr[32];
-        uint32_t pr[16];
         tmem_ld32(tdP + lane_off + c * 32, dr);
-        tmem_ld16(tS + lane_off + c * 16, pr);
         tmem_ld_wait(dr);
-        tmem_ld_wait(pr);
+        uint32_t ds[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(sd + c * 32 + j);
-          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pr[j / 2]));
-          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pr[j / 2 + 1]));
-          dsp[c][j / 2] = pack_bf16(p01.x * (__uint_as_float(dr[j + 0]) - d4.x),
-                                    p01.y * (__uint_as_float(dr[j + 1]) - d4.y));
-          dsp[c][j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
-                                        p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
+          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][j / 2]));
+          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][j / 2 + 1]));
+          ds[j / 2] = pack_bf16(p01.x * (__uint_as_float(dr[j + 0]) - d4.x),
+                                p01.y * (__uint_as_float(dr[j + 1]) - d4.y));
+          ds[j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
+                                    p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
         }
-        tmem_st16(tdP + lane_off + c * 16, dsp[c]);
+        tmem_st16(tdP + lane_off + c * 16, ds);
+        // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
+        // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          const int g = (c & 1) * 4 + g4;
+          st_shared_v4(row_base + (c >> 1) * 16384 + ((g ^ (kr & 7)) << 4), ds[4 * g4], ds[4 * g4 + 1],
+                       ds[4 * g4 + 2], ds[4 * g4 + 3]);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::bDSReady));
-
-      // dS (bf16) into shared memory as the MN-major A operand of the dQ MMA: row = key,
-      // 64-query chunks 16 KB apart, 16-byte granules XOR-swizzled by (key mod 8).
-      if (!(ok = mbar_wait_warp(bar(L::bDVDone), it & 1, ctl))) break;
-      const uint32_t row_base = sDS(s) + (uint32_t)kr * 128;
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int pi = h * 32 + g * 4;  // packed pair index of query 64h + 8g
-          const uint32_t* src = &dsp[pi >> 4][pi & 15];
-          st_shared_v4(row_base + h * 16384 + ((g ^ (kr & 7)) << 4), src[0], src[1], src[2], src[3]);
-        }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bSmemDS));
+      if (it + 1 < n_iter && !(ok = p_phase(it + 1))) break;
     }
     // ---------------------------------------------------------------- dK / dV epilogue
     if (ok) ok = mbar_wait_warp(bar(L::bFinal), 0, ctl);
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       uint32_t a[D / 32][32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tS + lane_off + c * 32, a[c]);
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tdP + lane_off + c * 32, a[c]);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) tmem_ld_wait(a[c]);
       tc_fence_before();
