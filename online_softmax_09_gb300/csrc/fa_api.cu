@@ -76,6 +76,19 @@ int make_map(CUtensorMap* m, const void* base, int d, int N, long long planes) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
 }
 
+// 2-D map over the fp32 dQ accumulator [rows][d]; box = 32 columns (128 B) x 32 rows,
+// 128-byte swizzle (the staging layout the backward's dQ drain writes).
+int make_map_dq(CUtensorMap* m, void* base, int d, long long rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
+}
+
 int check_sizes(int B, int Hq, int Hkv, int N, int d) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return FA_ERR_INVALID;
   if (Hq % Hkv != 0) return FA_ERR_INVALID;
@@ -167,20 +180,22 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
   uint32_t* status = nullptr;
   FA_TRY(current_device(&status));
-  CUtensorMap tq, tk, tv, tdo;
+  char* ws = static_cast<char*>(workspace);
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (stages & fa::kBwdCompute) {
     if (!load_encoder()) return FA_ERR_LAUNCH;
     FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
     FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
     FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
     FA_TRY(make_map(&tdo, dout, d, N, (long long)B * Hq));
+    FA_TRY(make_map_dq(&tdq, ws + w.dq_acc, d, (long long)B * Hq * fa::round_up_tile(N)));
   }
-  char* ws = static_cast<char*>(workspace);
   fa::BwdLaunch a;
   a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;
   a.tm_do = &tdo;
+  a.tm_dq = &tdq;
   a.o = o;
   a.dout = dout;
   a.lse = lse;

@@ -17,8 +17,8 @@
 //        MMA  dV += P_i^T dO_i ;  dP_i^T = V_n dO_i^T ;  S_{i+1}^T = K_n Q_{i+1}^T
 //        softmax warps: dS_i^T = P_i^T (dP_i^T - delta), bf16 -> TMEM and -> shared memory
 //        MMA  dK += dS_i^T Q_i ;  dQ_i = dS_i K_n  (into the dP^T columns, now free)
-//        drain warps (thread = query row): dQ_i TMEM -> fp32 red.global.add into the
-//        workspace accumulator.
+//        drain warps (thread = query row): dQ_i TMEM -> shared memory -> bulk tensor
+//        reduction (add) into the fp32 workspace accumulator.
 //      The next tile's S^T is computed while the softmax warps work on dS_i, and its P while
 //      the dK and dQ MMAs run, so the tensor core does not wait for the softmax warps.
 //   3. dQ conversion: dq = bf16(scale * accumulator).
@@ -129,7 +129,9 @@ struct BwdSmem {
   static constexpr int kStD = 2 * kTileBytes + 512;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kDS = kStage0 + 2 * kStageBytes;
-  static constexpr int kBar = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
+  // dQ staging for the bulk reductions: 4 drain warps x 32 rows x 128 bytes.
+  static constexpr int kDQ = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
+  static constexpr int kBar = kDQ + 4 * 32 * 128;
   enum {
     bKV = 0,
     bQFull = 1,       // 2
@@ -150,7 +152,8 @@ struct BwdSmem {
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kStageBytes % 1024 == 0 && kStage0 % 1024 == 0 && kDS % 1024 == 0, "1024-byte alignment");
+  static_assert(kStageBytes % 1024 == 0 && kStage0 % 1024 == 0 && kDS % 1024 == 0 && kDQ % 1024 == 0,
+                "1024-byte alignment");
 };
 
 constexpr int kBwdThreads = 320;
@@ -159,7 +162,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -222,6 +225,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -464,8 +468,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ dQ drain warps 6-9
+    // Each warp owns 32 query rows (its TMEM lane quarter). dQ_i leaves TMEM at once (so the
+    // next dP MMA can reuse the columns); then, 32 columns at a time, the warp stages its
+    // 32 x 32 fp32 block in shared memory (128-byte swizzled: 16-byte granule g of row r at
+    // g ^ (r mod 8)) and one lane adds it into the workspace accumulator with a bulk tensor
+    // reduction. Warps never wait for one another.
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int qr = (warp & 3) * 32 + lane;  // query row within the tile (TMEM lane)
+    const uint32_t stage_buf = sbase + L::kDQ + (uint32_t)(warp & 3) * 4096;
+    const uint32_t my_row = stage_buf + (uint32_t)lane * 128;
     for (int it = 0; it < n_iter; ++it) {
       int hq, i;
       item(it, hq, i);
@@ -478,14 +488,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = 0; c < D / 32; ++c) tmem_ld_wait(a[c]);
       tc_fence_before();
       mbar_arrive(bar(L::bDQFree));
-      float* dst = p.dq_acc + ((size_t)(b * p.Hq + hq) * p.Npad + (size_t)i * kTile + qr) * D;
+      const int row0 = (b * p.Hq + hq) * p.Npad + i * kTile + (warp & 3) * 32;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c)
+      for (int c = 0; c < D / 32; ++c) {
+        if (lane == 0) bulk_wait_read_all();  // the previous block has left the staging buffer
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          red_add_v4(dst + c * 32 + j, __uint_as_float(a[c][j]), __uint_as_float(a[c][j + 1]),
-                     __uint_as_float(a[c][j + 2]), __uint_as_float(a[c][j + 3]));
+        for (int g = 0; g < 8; ++g)
+          st_shared_v4(my_row + ((g ^ (lane & 7)) << 4), a[c][4 * g], a[c][4 * g + 1], a[c][4 * g + 2],
+                       a[c][4 * g + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&tm_dq, stage_buf, c * 32, row0);
+          bulk_commit_group();
+        }
+      }
     }
+    if (lane == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
   }
 
   // ------------------------------------------------------------------ teardown
@@ -533,7 +553,8 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
     const long long grid = (long long)a.B * a.Hkv * T;
-    fa_bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, p);
+    fa_bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do,
+                                                                          *a.tm_dq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

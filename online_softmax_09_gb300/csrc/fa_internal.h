@@ -28,6 +28,7 @@ struct BwdLaunch {
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_do;
+  const CUtensorMap* tm_dq;  // fp32 dQ accumulator viewed as [B*Hq*Npad][d], box 32 x 32
   const void* o;
   const void* dout;
   const float* lse;
