@@ -67,13 +67,17 @@ constexpr int kFwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kNegInf = 0xff800000u;
 
-__device__ __forceinline__ float max32(const uint32_t (&s)[32]) {
+// Maximum of 64 values held in two 32-register chunks (three-input max, 8 partial maxima).
+__device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (&b)[32], float init) {
   float m[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(s[i]), __uint_as_float(s[i + 8]));
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], fmaxf(__uint_as_float(s[i + 16]), __uint_as_float(s[i + 24])));
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+  for (int k = 0; k < 8; ++k) {
+    m[k] = max3f(__uint_as_float(a[k]), __uint_as_float(a[k + 8]), __uint_as_float(a[k + 16]));
+    m[k] = max3f(m[k], __uint_as_float(a[k + 24]), __uint_as_float(b[k]));
+    m[k] = max3f(m[k], __uint_as_float(b[k + 8]), __uint_as_float(b[k + 16]));
+    m[k] = fmaxf(m[k], __uint_as_float(b[k + 24]));
+  }
+  return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), max3f(m[6], m[7], init));
 }
 
 // Columns past `lim` (the last visible key of this row within the tile) become -inf.
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mask32(a, c * 32, lim);
           mask32(b2, (c + 1) * 32, lim);
         }
-        mx = fmaxf(mx, fmaxf(max32(a), max32(b2)));
+        mx = max64(a, b2, mx);
       }
       // Running max in base-2 units; correction exp(m_old - m_new) (0 on the first tile).
       const float m_new = fmaxf(m_run, mx * sl2);
@@ -311,13 +315,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                    make_float2(corr, corr));
+              o[i] = __float_as_uint(r.x);
+              o[i + 1] = __float_as_uint(r.y);
+            }
             tmem_st32(tO + c * 32, o);
           }
         }
       }
       // Pass 2: P = 2^(S*scale*log2e - m) as bf16 over the S columns already read, and row sum.
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-m_use, -m_use);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t a[32];
@@ -327,15 +338,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(a[i]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(a[i + 1]), sl2, -m_use));
-          sum[(i >> 1) & 3] += p0 + p1;
-          pk[i >> 1] = pack_bf16(p0, p1);
+          const float2 x = fma2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sl2x2, negm);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          sum[(i >> 1) & 1] = add2(sum[(i >> 1) & 1], pp);
+          pk[i >> 1] = pack_bf16(pp.x, pp.y);
         }
         // P chunk c covers columns [16c, 16c+16): S columns that pass 2 has already read.
         tmem_st16(tS + c * 16, pk);
       }
-      l_run = l_run * corr + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      l_run = l_run * corr + ((sum[0].x + sum[1].x) + (sum[0].y + sum[1].y));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(L::bPFull + t));
@@ -354,8 +365,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint4 w[4];
         uint32_t* wp = reinterpret_cast<uint32_t*>(w);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          wp[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        for (int i = 0; i < 16; ++i) {
+          const float2 r = mul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                                make_float2(inv_l, inv_l));
+          wp[i] = pack_bf16(r.x, r.y);
+        }
         if (row < p.N) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + row_off + c * 32);
 #pragma unroll
