@@ -17,6 +17,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool init = false;
   bool supported = false;
+  int num_sms = 0;
   uint32_t* status = nullptr;  // device address of g_fa_status on this device
 };
 DeviceState g_devices[kMaxDevices];
@@ -27,7 +28,7 @@ std::once_flag g_encode_once;
 
 // Looks up (once per device, with that device current) whether it is an sm_103 part and the
 // device address of its status word.
-int current_device(uint32_t** status) {
+int current_device(uint32_t** status, int* num_sms = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_DEVICE;
@@ -39,6 +40,7 @@ int current_device(uint32_t** status) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FA_ERR_LAUNCH;
     s.supported = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_LAUNCH;
     if (s.supported) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
@@ -48,6 +50,7 @@ int current_device(uint32_t** status) {
   }
   if (!s.supported) return FA_ERR_DEVICE;
   if (status) *status = s.status;
+  if (num_sms) *num_sms = s.num_sms;
   return FA_OK;
 }
 
@@ -137,7 +140,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   FA_TRY(check_ptr(lse));
   if (counters != nullptr && (reinterpret_cast<uintptr_t>(counters) & 7u)) return FA_ERR_ALIGN;
   uint32_t* status = nullptr;
-  FA_TRY(current_device(&status));
+  int num_sms = 0;
+  FA_TRY(current_device(&status, &num_sms));
   if (!load_encoder()) return FA_ERR_LAUNCH;
   CUtensorMap tq, tk, tv;
   FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
@@ -157,6 +161,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.N = N;
   a.d = d;
   a.causal = causal ? 1 : 0;
+  a.num_sms = num_sms;
   a.scale = resolve_scale(scale, d);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return fa::launch_fwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

@@ -1,7 +1,9 @@
 // fa_fwd.cu -- forward pass of exact softmax attention on sm_103a.
 //
-// One CTA computes two 128-row query tiles (256 consecutive rows) of one (batch, query head);
-// both tiles share every K/V tile loaded:
+// Persistent kernel: one CTA per SM walks a list of work items (longest first for causal).
+// An item is two 128-row query tiles (256 consecutive rows) of one (batch, query head); both
+// tiles share every K/V tile loaded. The next item's Q loads and score MMAs start while the
+// previous item's epilogue is still writing O. Roles:
 //   warp 8      TMA producer: Q0, Q1 once, then K_j into an NK-stage ring and V_j into an
 //               NV-stage ring.
 //   warp 9      MMA issuer (one thread) and TMEM owner. Issue order per key tile j:
@@ -35,9 +37,42 @@ struct FwdParams {
   uint32_t* status;
   int B, Hq, Hkv, N, causal;
   int num_tiles;     // ceil(N / 128): query tiles per head == key tiles per head
-  int num_pairs;     // ceil(num_tiles / 2): CTAs per head
+  int num_pairs;     // ceil(num_tiles / 2): work items per head
+  int num_items;     // num_pairs * B * Hq
   float scale_log2;  // scale * log2(e)
 };
+
+// One work item: query tiles 2*pair and 2*pair+1 of head bh. Items are numbered so that, for
+// causal attention, the longest come first (item k -> pair num_pairs-1-k/BH).
+struct FwdItem {
+  int bh, kv_z, qt0, n0, n1, n_max;
+  bool has1;
+};
+// Item of this CTA in round r: items are dealt in rounds of gridDim.x, snake order (CTA c gets
+// item r*G + c in even rounds and r*G + G-1-c in odd rounds), which balances the linearly
+// decreasing causal item lengths across CTAs. Returns -1 past the end.
+__device__ __forceinline__ int fwd_item_index(int r, int num_items) {
+  const int G = gridDim.x;
+  const int k = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return k < num_items ? k : -1;
+}
+
+__device__ __forceinline__ FwdItem fwd_item(int k, const FwdParams& p) {
+  FwdItem it;
+  const int BH = p.B * p.Hq;
+  const int rank = k / BH;
+  it.bh = k - rank * BH;
+  const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
+  const int b = it.bh / p.Hq;
+  const int hq = it.bh - b * p.Hq;
+  it.kv_z = b * p.Hkv + hq / (p.Hq / p.Hkv);
+  it.qt0 = 2 * pair;
+  it.has1 = it.qt0 + 1 < p.num_tiles;
+  it.n0 = p.causal ? (it.qt0 + 1) : p.num_tiles;  // key tiles each query tile visits
+  it.n1 = it.has1 ? (p.causal ? (it.qt0 + 2) : p.num_tiles) : 0;
+  it.n_max = it.has1 ? it.n1 : it.n0;
+  return it;
+}
 
 template <int D, int NK, int NV>
 struct FwdSmem {
@@ -55,7 +90,9 @@ struct FwdSmem {
   static constexpr int bSFull = bVEmpty + NV; // 2 (per tile)
   static constexpr int bPFull = bSFull + 2;   // 2
   static constexpr int bOFull = bPFull + 2;   // 2
-  static constexpr int bDrain = bOFull + 2;
+  static constexpr int bQEmpty = bOFull + 2;  // 2: Q buffer t no longer read by MMAs
+  static constexpr int bOFree = bQEmpty + 2;  // 2: O_t read out by the epilogue
+  static constexpr int bDrain = bOFree + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -107,27 +144,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: query tiles 2*pair and 2*pair+1 of head bh. Causal pairs run longest first.
-  const int BH = p.B * p.Hq;
-  const int rank = blockIdx.x / BH;
-  const int bh = blockIdx.x - rank * BH;
-  const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
-  const int b = bh / p.Hq;
-  const int hq = bh - b * p.Hq;
-  const int kv_z = b * p.Hkv + hq / (p.Hq / p.Hkv);
-  const int qt0 = 2 * pair;
-  const bool has1 = qt0 + 1 < p.num_tiles;
-  // Key tiles each query tile visits.
-  const int n0 = p.causal ? (qt0 + 1) : p.num_tiles;
-  const int n1 = has1 ? (p.causal ? (qt0 + 2) : p.num_tiles) : 0;
-  const int n_max = has1 ? n1 : n0;
-
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::bQ + t), 1);
       mbar_init(bar(L::bSFull + t), 1);
       mbar_init(bar(L::bPFull + t), 128);
       mbar_init(bar(L::bOFull + t), 1);
+      mbar_init(bar(L::bQEmpty + t), 1);
+      mbar_init(bar(L::bOFree + t), 128);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(L::bKFull + s), 1);
@@ -155,39 +179,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Persistent CTAs: every role walks the same item sequence (fwd_item_index) and keeps running
+  // counts, from which all barrier phases follow.
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       constexpr uint32_t kBytes = L::kTileBytes;
-      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-        mbar_expect_tx(bar(L::bQ + t), kBytes);
+      uint32_t gk = 0, gv = 0;  // K and V tiles loaded so far
+      uint32_t qn[2] = {0, 0};  // Q loads into each buffer so far
+      bool ok = true;
+      for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+        const int k = fwd_item_index(r, p.num_items);
+        if (k < 0) continue;
+        const FwdItem it = fwd_item(k, p);
+        for (int t = 0; t < (it.has1 ? 2 : 1); ++t) {
+          if (!(ok = mbar_wait(bar(L::bQEmpty + t), (qn[t] & 1) ^ 1, ctl))) break;
+          mbar_expect_tx(bar(L::bQ + t), kBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sQ + t * kBytes + c * 16384, &tm_q, bar(L::bQ + t), c * 64, (qt0 + t) * kTile, bh);
-      }
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_max; ++j) {
-        const int sk = j % NK, sv = j % NV;
-        if (!mbar_wait(bar(L::bKEmpty + sk), ((j / NK) & 1) ^ 1, ctl)) break;
-        mbar_expect_tx(bar(L::bKFull + sk), kBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sQ + t * kBytes + c * 16384, &tm_q, bar(L::bQ + t), c * 64, (it.qt0 + t) * kTile, it.bh);
+          ++qn[t];
+        }
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          const uint32_t sk = gk % NK, sv = gv % NV;
+          if (!(ok = mbar_wait(bar(L::bKEmpty + sk), ((gk / NK) & 1) ^ 1, ctl))) break;
+          mbar_expect_tx(bar(L::bKFull + sk), kBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sK + sk * kBytes + c * 16384, &tm_k, bar(L::bKFull + sk), c * 64, j * kTile, kv_z);
-        k_issued = j + 1;
-        if (!mbar_wait(bar(L::bVEmpty + sv), ((j / NV) & 1) ^ 1, ctl)) break;
-        mbar_expect_tx(bar(L::bVFull + sv), kBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sK + sk * kBytes + c * 16384, &tm_k, bar(L::bKFull + sk), c * 64, j * kTile, it.kv_z);
+          ++gk;
+          if (!(ok = mbar_wait(bar(L::bVEmpty + sv), ((gv / NV) & 1) ^ 1, ctl))) break;
+          mbar_expect_tx(bar(L::bVFull + sv), kBytes);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sV + sv * kBytes + c * 16384, &tm_v, bar(L::bVFull + sv), c * 64, j * kTile, kv_z);
-        v_issued = j + 1;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sV + sv * kBytes + c * 16384, &tm_v, bar(L::bVFull + sv), c * 64, j * kTile, it.kv_z);
+          ++gv;
+        }
       }
       if (*abort_flag) {  // let every copy still in flight land before shared memory is freed
-        drain_wait(bar(L::bQ), 0);
-        if (has1) drain_wait(bar(L::bQ + 1), 0);
-        for (int j = k_issued > NK ? k_issued - NK : 0; j < k_issued; ++j)
-          drain_wait(bar(L::bKFull + j % NK), (j / NK) & 1);
-        for (int j = v_issued > NV ? v_issued - NV : 0; j < v_issued; ++j)
-          drain_wait(bar(L::bVFull + j % NV), (j / NV) & 1);
+        for (int t = 0; t < 2; ++t)
+          if (qn[t] > 0) drain_wait(bar(L::bQ + t), (qn[t] - 1) & 1);
+        for (uint32_t g = gk > NK ? gk - NK : 0; g < gk; ++g) drain_wait(bar(L::bKFull + g % NK), (g / NK) & 1);
+        for (uint32_t g = gv > NV ? gv - NV : 0; g < gv; ++g) drain_wait(bar(L::bVFull + g % NV), (g / NV) & 1);
       }
     }
   } else if (warp == 9) {
@@ -195,9 +228,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      auto issue_s = [&](int t, int j) -> bool {
-        const int sk = j % NK;
-        if (!mbar_wait(bar(L::bKFull + sk), (j / NK) & 1, ctl)) return false;
+      uint32_t gk = 0, gv = 0;  // K and V tiles consumed so far
+      uint32_t qn[2] = {0, 0};  // items that used query tile t
+      uint32_t pc[2] = {0, 0};  // P.V MMAs issued for tile t
+      auto issue_s = [&](int t, uint32_t g) -> bool {  // S_t = Q_t K^T with K tile number g
+        const uint32_t sk = g % NK;
+        if (!mbar_wait(bar(L::bKFull + sk), (g / NK) & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t q_base = sQ + t * L::kTileBytes;
         const uint32_t k_base = sK + sk * L::kTileBytes;
@@ -211,45 +247,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(bar(L::bSFull + t));
         return true;
       };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int sv = j % NV;
-        if (!mbar_wait(bar(L::bPFull + t), j & 1, ctl)) return false;
-        if (!mbar_wait(bar(L::bVFull + sv), (j / NV) & 1, ctl)) return false;
+      auto issue_pv = [&](int t, uint32_t g, bool first) -> bool {  // O_t += P_t V, V tile number g
+        const uint32_t sv = g % NV;
+        if (!mbar_wait(bar(L::bPFull + t), pc[t] & 1, ctl)) return false;
+        if (!mbar_wait(bar(L::bVFull + sv), (g / NV) & 1, ctl)) return false;
+        // The first P.V of an item overwrites O_t: the previous item's epilogue must be done.
+        if (first && qn[t] > 1 && !mbar_wait(bar(L::bOFree + t), (qn[t] - 2) & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t v_base = sV + sv * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           // V as the MN-major B operand: 16 keys = 2 swizzle atoms of 8 rows x 128 B.
           mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024),
-                 idO, (j > 0 || kk > 0));
+                 idO, (!first || kk > 0));
         }
         mma_commit(bar(L::bOFull + t));
+        ++pc[t];
         return true;
       };
-      bool ok = mbar_wait(bar(L::bQ), 0, ctl);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_s(0, 0);
-      }
-      if (ok && has1) {
-        ok = mbar_wait(bar(L::bQ + 1), 0, ctl);
-        if (ok) {
+      bool ok = true;
+      for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+        const int k = fwd_item_index(r, p.num_items);
+        if (k < 0) continue;
+        const FwdItem it = fwd_item(k, p);
+        for (int t = 0; ok && t < (it.has1 ? 2 : 1); ++t) {
+          if (!(ok = mbar_wait(bar(L::bQ + t), qn[t] & 1, ctl))) break;
+          ++qn[t];
           tc_fence_after();
-          ok = issue_s(1, 0);
+          if (!(ok = issue_s(t, gk))) break;
+          if ((t ? it.n1 : it.n0) == 1) mma_commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
         }
-      }
-      if (ok) mma_commit(bar(L::bKEmpty));  // K_0 released once both score MMAs complete
-      for (int j = 0; ok && j < n_max; ++j) {
-        if (j < n0) {
-          if (!(ok = issue_pv(0, j))) break;
-          if (j + 1 < n0 && !(ok = issue_s(0, j + 1))) break;
+        if (!ok) break;
+        mma_commit(bar(L::bKEmpty + gk % NK));  // K tile 0 of the item: both score MMAs issued
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          if (j < it.n0) {
+            if (!(ok = issue_pv(0, gv + j, j == 0))) break;
+            if (j + 1 < it.n0) {
+              if (!(ok = issue_s(0, gk + j + 1))) break;
+              if (j + 2 == it.n0) mma_commit(bar(L::bQEmpty));
+            }
+          }
+          if (j < it.n1) {
+            if (!(ok = issue_pv(1, gv + j, j == 0))) break;
+            if (j + 1 < it.n1) {
+              if (!(ok = issue_s(1, gk + j + 1))) break;
+              if (j + 2 == it.n1) mma_commit(bar(L::bQEmpty + 1));
+            }
+          }
+          mma_commit(bar(L::bVEmpty + (gv + j) % NV));
+          if (j + 1 < it.n_max) mma_commit(bar(L::bKEmpty + (gk + j + 1) % NK));
         }
-        if (j < n1) {
-          if (!(ok = issue_pv(1, j))) break;
-          if (j + 1 < n1 && !(ok = issue_s(1, j + 1))) break;
-        }
-        mma_commit(bar(L::bVEmpty + j % NV));
-        if (j + 1 < n_max) mma_commit(bar(L::bKEmpty + (j + 1) % NK));
+        gk += it.n_max;
+        gv += it.n_max;
       }
       if (*abort_flag) {  // wait for issued MMAs before tensor memory is released
         mma_commit(bar(L::bDrain));
@@ -258,134 +307,145 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
-    const int t = warp >> 2;  // query tile of this warpgroup
-    const int n_kv = t ? n1 : n0;
-    const int qt = qt0 + t;
+    const int t = warp >> 2;  // query tile of this warpgroup within an item
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128 * t + lane_off;
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
-    const int row = qt * kTile + (threadIdx.x & 127);
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;
-    float l_run = 0.f;
-    uint32_t n_rescaled = 0;
+    uint32_t sc = 0;  // score tiles of this query tile processed so far (all items)
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(bar(L::bSFull + t), j & 1, ctl)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int kv0 = j * kTile;
-      const bool need_mask = (p.causal && j == qt) || kv0 + kTile > p.N;
-      const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;  // last visible column
-      // Pass 1: row max.
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t a[32], b2[32];
-        tmem_ld32(tS + c * 32, a);
-        tmem_ld32(tS + (c + 1) * 32, b2);
-        tmem_ld_wait(a);
-        tmem_ld_wait(b2);
-        if (need_mask) {
-          mask32(a, c * 32, lim);
-          mask32(b2, (c + 1) * 32, lim);
-        }
-        mx = max64(a, b2, mx);
-      }
-      // Running max in base-2 units; correction exp(m_old - m_new) (0 on the first tile).
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const float corr = (m_new > m_run) ? ex2(m_run - m_new) : 1.f;
-      if (j > 0 && m_new > m_run && row < p.N) ++n_rescaled;
-      m_run = m_new;
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      if (j > 0) {
-        // O += P_{j-1} V_{j-1} has completed before S_j did; this wait at every tile keeps the
-        // warp's view of the barrier phase exact and returns at once.
-        if (!mbar_wait_warp(bar(L::bOFull + t), (j - 1) & 1, ctl)) {
+    for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+        const int k = fwd_item_index(r, p.num_items);
+        if (k < 0) continue;
+      const FwdItem itm = fwd_item(k, p);
+      const int n_kv = t ? itm.n1 : itm.n0;
+      if (n_kv == 0) continue;
+      const int qt = itm.qt0 + t;
+      const int row = qt * kTile + (threadIdx.x & 127);
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      uint32_t n_rescaled = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!mbar_wait_warp(bar(L::bSFull + t), (sc + j) & 1, ctl)) {
           ok = false;
           break;
         }
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
-          tc_fence_after();
+        tc_fence_after();
+        const int kv0 = j * kTile;
+        const bool need_mask = (p.causal && j == qt) || kv0 + kTile > p.N;
+        const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;  // last visible column
+        // Pass 1: row max.
+        float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t a[32], b2[32];
+          tmem_ld32(tS + c * 32, a);
+          tmem_ld32(tS + (c + 1) * 32, b2);
+          tmem_ld_wait(a);
+          tmem_ld_wait(b2);
+          if (need_mask) {
+            mask32(a, c * 32, lim);
+            mask32(b2, (c + 1) * 32, lim);
+          }
+          mx = max64(a, b2, mx);
+        }
+        // Running max in base-2 units; correction exp(m_old - m_new) (0 on the first tile).
+        const float m_new = fmaxf(m_run, mx * sl2);
+        const float corr = (m_new > m_run) ? ex2(m_run - m_new) : 1.f;
+        if (j > 0 && m_new > m_run && row < p.N) ++n_rescaled;
+        m_run = m_new;
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        if (j > 0) {
+          // O += P_{j-1} V has completed before S_j did; this wait at every tile keeps the
+          // warp's view of the barrier phase exact and returns at once.
+          if (!mbar_wait_warp(bar(L::bOFull + t), (sc + j - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          if (__any_sync(0xffffffffu, corr != 1.f)) {
+            tc_fence_after();
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
-                                    make_float2(corr, corr));
-              o[i] = __float_as_uint(r.x);
-              o[i + 1] = __float_as_uint(r.y);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                      make_float2(corr, corr));
+                o[i] = __float_as_uint(r.x);
+                o[i + 1] = __float_as_uint(r.y);
+              }
+              tmem_st32(tO + c * 32, o);
             }
-            tmem_st32(tO + c * 32, o);
           }
         }
-      }
-      // Pass 2: P = 2^(S*scale*log2e - m) as bf16 over the S columns already read, and row sum.
-      float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      const float2 sl2x2 = make_float2(sl2, sl2);
-      const float2 negm = make_float2(-m_use, -m_use);
+        // Pass 2: P = 2^(S*scale*log2e - m) as bf16 over the S columns already read, and row sum.
+        float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-m_use, -m_use);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tS + c * 32, a);
-        tmem_ld_wait(a);
-        if (need_mask) mask32(a, c * 32, lim);
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tS + c * 32, a);
+          tmem_ld_wait(a);
+          if (need_mask) mask32(a, c * 32, lim);
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = fma2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sl2x2, negm);
-          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-          sum[(i >> 1) & 1] = add2(sum[(i >> 1) & 1], pp);
-          pk[i >> 1] = pack_bf16(pp.x, pp.y);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = fma2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sl2x2, negm);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum[(i >> 1) & 1] = add2(sum[(i >> 1) & 1], pp);
+            pk[i >> 1] = pack_bf16(pp.x, pp.y);
+          }
+          // P chunk c covers columns [16c, 16c+16): S columns that pass 2 has already read.
+          tmem_st16(tS + c * 16, pk);
         }
-        // P chunk c covers columns [16c, 16c+16): S columns that pass 2 has already read.
-        tmem_st16(tS + c * 16, pk);
+        l_run = l_run * corr + ((sum[0].x + sum[1].x) + (sum[0].y + sum[1].y));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(L::bPFull + t));
       }
-      l_run = l_run * corr + ((sum[0].x + sum[1].x) + (sum[0].y + sum[1].y));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(L::bPFull + t));
-    }
-    // ---------------------------------------------------------------- epilogue
-    if (ok && n_kv > 0) ok = mbar_wait_warp(bar(L::bOFull + t), (n_kv - 1) & 1, ctl);
-    if (ok && n_kv > 0) {
+      if (!ok) break;
+      // ---------------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait_warp(bar(L::bOFull + t), (sc + n_kv - 1) & 1, ctl))) break;
+      sc += n_kv;
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      const size_t row_off = ((size_t)bh * p.N + row) * D;
+      uint4 w[D / 32][4];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait(o);
-        uint4 w[4];
-        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+        uint32_t* wp = reinterpret_cast<uint32_t*>(w[c]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 r = mul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
                                 make_float2(inv_l, inv_l));
           wp[i] = pack_bf16(r.x, r.y);
         }
-        if (row < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + row_off + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = w[i];
-        }
       }
-      if (row < p.N) p.lse[(size_t)bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
-    }
-    if (p.counters != nullptr && n_kv > 0) {
-      unsigned int r = n_rescaled;
+      // O_t has been read: the next item's first P.V may overwrite it.
+      tc_fence_before();
+      mbar_arrive(bar(L::bOFree + t));
+      if (row < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)itm.bh * p.N + row) * D);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-      if (lane == 0 && r) atomicAdd(&p.counters[2], (unsigned long long)r);
-      if ((threadIdx.x & 127) == 0) {
-        atomicAdd(&p.counters[0], (unsigned long long)n_kv);
-        atomicAdd(&p.counters[1], (unsigned long long)(p.num_tiles - n_kv));
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[c * 4 + i] = w[c][i];
+        p.lse[(size_t)itm.bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
+      }
+      if (p.counters != nullptr) {
+        unsigned int r = n_rescaled;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+        if (lane == 0 && r) atomicAdd(&p.counters[2], (unsigned long long)r);
+        if ((threadIdx.x & 127) == 0) {
+          atomicAdd(&p.counters[0], (unsigned long long)n_kv);
+          atomicAdd(&p.counters[1], (unsigned long long)(p.num_tiles - n_kv));
+        }
       }
     }
   }
@@ -406,8 +466,8 @@ static cudaError_t launch_fwd_t(const FwdLaunch& a, const FwdParams& p) {
   cudaError_t e =
       cudaFuncSetAttribute(fa_fwd_kernel<D, NK, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.num_pairs * p.B * p.Hq;
-  fa_fwd_kernel<D, NK, NV><<<(unsigned)grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+  const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
+  fa_fwd_kernel<D, NK, NV><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
   return cudaGetLastError();
 }
 
@@ -424,6 +484,7 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.causal = a.causal;
   p.num_tiles = (a.N + kTile - 1) / kTile;
   p.num_pairs = (p.num_tiles + 1) / 2;
+  p.num_items = p.num_pairs * a.B * a.Hq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   if (a.d == 128) return launch_fwd_t<128, 3, 2>(a, p);
   return launch_fwd_t<64, 4, 4>(a, p);

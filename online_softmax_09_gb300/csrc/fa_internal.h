@@ -18,6 +18,7 @@ struct FwdLaunch {
   unsigned long long* counters;  // nullable
   uint32_t* status;
   int B, Hq, Hkv, N, d, causal;
+  int num_sms;  // persistent grid size
   float scale;
   cudaStream_t stream;
 };
