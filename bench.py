@@ -86,6 +86,18 @@ def measured_traffic():
     return rec.get("dram_bytes_per_launch")
 
 
+def rank_max(value, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (the timing rule: the slowest rank sets the time).
+    Identity without a process group."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -211,10 +223,7 @@ def run_ours(args):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_compute_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[4]) for e in evs)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = rank_max(total_ms, dist, dev)
 
     e2e = None
     if not args.no_e2e:
@@ -243,11 +252,7 @@ def run_ours(args):
         a1.record(stream)
         torch.cuda.synchronize()
         fa.check()
-        e2e_ms = a0.elapsed_time(a1) / E
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = rank_max(a0.elapsed_time(a1) / E, dist, dev)
         e2e = {"value": round(world * f_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
