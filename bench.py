@@ -388,6 +388,60 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------------------------
+# Extra workloads (not the headline metric): one JSON line each, same timing rules.
+# --------------------------------------------------------------------------------------------
+def load_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_softmax_rows(args):
+    """Online-softmax rows (fa_softmax_rows): 65536 rows x 2048 fp32 logits, N(0,1)*8 from seed 3
+    (the shape of the pages' check, scaled up to be HBM-sized: 512 MiB in, 512 MiB out)."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+
+    rows, n = 65536, 2048
+    g = torch.Generator().manual_seed(3)
+    xh = torch.randn(rows, n, generator=g) * 8.0
+    x = xh.cuda()
+    p = torch.empty_like(x)
+    lse = torch.empty(rows, device=x.device)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        fa.softmax_rows(x, out=p, lse=lse)
+    fa.check()
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        fa.softmax_rows(x, out=p, lse=lse)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    fa.check()
+    ms = t0.elapsed_time(t1) / K
+    nbytes = rows * n * 8 + rows * 4  # read x, write p and lse
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, src = load_hbm_peak()
+    print(json.dumps({
+        "metric": "online softmax rows GB/s (fp32, 65536 x 2048, read x + write p + lse)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "fa_softmax_rows 65536 x 2048, N(0,1)*8 seed 3",
+                   "l2": "inputs larger than L2 (512 MiB), no flush"},
+        "roofline": {"kernel": "fa_softmax_warp_rows_kernel<16>", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "peak_source": f"{src} hbm_gbs (copy)",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": K}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -398,10 +452,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
+    ap.add_argument("--workload", choices=["attention", "softmax_rows"], default="attention",
+                    help="attention (the headline metric) or one of the extra workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.workload == "softmax_rows":
+        run_softmax_rows(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

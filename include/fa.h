@@ -149,6 +149,18 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    fa_stream_t stream);
 
 /*
+ * Row-wise softmax by the online normaliser ("LLM Architecture Refresh [3]", section 2, "Online
+ * softmax: the one idea", and section 3, "Partial softmaxes compose"): for each row of x,
+ * a running max m and sum l = sum exp(x - m) are carried in one pass, partial (m, l) pairs are
+ * merged by rebasing to the larger max, then p = exp(x - m) / l and lse = m + ln l.
+ *   x, p : [rows][n] fp32, device, 16-byte aligned, not overlapping.
+ *   lse  : [rows] fp32, device, or NULL.
+ * Entries equal to -inf get p = 0 (masked logits); a row with no finite entry is undefined.
+ * Rows of up to 8192 elements (n a multiple of 4) are read once; longer rows twice.
+ */
+int fa_softmax_rows(const float *x, float *p, float *lse, long long rows, int n, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status word:
  * FA_OK, FA_ERR_TIMEOUT (a kernel gave up waiting) or FA_ERR_LAUNCH (the stream reported
  * a CUDA error).

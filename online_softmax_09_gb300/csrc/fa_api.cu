@@ -268,6 +268,17 @@ int fa_bwd_finalize(void* dq, void* workspace, size_t workspace_bytes, int B, in
                   workspace_bytes, B, Hq, Hkv, N, d, 0, scale, stream, fa::kBwdFinalize);
 }
 
+int fa_softmax_rows(const float* x, float* p, float* lse, long long rows, int n, fa_stream_t stream) {
+  if (rows < 1 || rows > 0x7fffffffLL || n < 1) return FA_ERR_INVALID;
+  FA_TRY(check_ptr(x));
+  FA_TRY(check_ptr(p));
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_ALIGN;
+  FA_TRY(current_device(nullptr));
+  return fa::launch_softmax_rows(x, p, lse, rows, n, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
 int fa_check(fa_stream_t stream) {
   uint32_t* status = nullptr;
   int r = current_device(&status);

@@ -49,6 +49,9 @@ struct BwdLaunch {
 enum : int { kBwdPrepare = 1, kBwdCompute = 2, kBwdFinalize = 4, kBwdAll = 7 };
 cudaError_t launch_bwd(const BwdLaunch& a, int stages);
 
+// Row-wise online softmax: x, p [rows][n] fp32, lse [rows] (nullable).
+cudaError_t launch_softmax_rows(const float* x, float* p, float* lse, long long rows, int n, cudaStream_t st);
+
 inline int round_up_tile(int n) { return (n + kTile - 1) / kTile * kTile; }
 
 }  // namespace fa

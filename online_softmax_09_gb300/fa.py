@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_compute.restype = _i
         L.fa_bwd_finalize.argtypes = [_vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd_finalize.restype = _i
+        L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]
+        L.fa_softmax_rows.restype = _i
         L.fa_check.argtypes = [_vp]
         L.fa_check.restype = _i
         L.fa_strerror.argtypes = [_i]
@@ -150,6 +152,22 @@ def backward_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, causal: bool = F
     if between is not None:
         between(3)
     return dq, dk, dv
+
+
+def softmax_rows(x, out=None, lse=None, with_lse: bool = True, stream=None):
+    """Row-wise online softmax of a contiguous fp32 CUDA tensor [..., n] (fa_softmax_rows)."""
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    n = x.shape[-1]
+    rows = x.numel() // n
+    p = out if out is not None else torch.empty_like(x)
+    l = lse if lse is not None else (torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+                                     if with_lse else None)
+    r = lib().fa_softmax_rows(x.data_ptr(), p.data_ptr(), l.data_ptr() if l is not None else None, rows, n,
+                              _stream_handle(stream, x.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_softmax_rows")
+    return p, l
 
 
 def check(stream=None, device=None) -> None:
