@@ -69,6 +69,34 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            fa_stream_t stream);
 
 /*
+ * Forward pass with a causal sliding window of `window` keys: query i sees keys
+ * i - window < j <= i ("LLM Architecture Refresh [3]", section 5, sliding_window_attention:
+ * keys older than i - window + 1 or in the future are masked). Key tiles wholly outside every
+ * row's window are skipped on both sides. window >= 1 (window >= N is plain causal).
+ * Same arguments, layouts and errors as fa_fwd otherwise. Extra device memory: none.
+ */
+int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int N, int d, int window, float scale,
+                  fa_stream_t stream);
+
+/*
+ * Split-KV forward: the key tiles of every pair of query tiles are divided into num_splits
+ * ranges processed by different CTAs, each writing a partial output and its LSE; a merge
+ * kernel combines them by the rule that partial softmaxes compose ("LLM Architecture
+ * Refresh [3]", section 3): with w_s = exp(LSE_s - max_s LSE_s),
+ * O = sum_s w_s O_s / sum_s w_s and LSE = max_s LSE_s + ln(sum_s w_s). Fills the GPU when
+ * B * Hq * ceil(N / 256) is below the SM count.
+ *   num_splits : 1..64, or <= 0 to let the library choose (it picks 1 when the GPU is full).
+ *   workspace  : device, 16-byte aligned, >= fa_fwd_splitkv_workspace_bytes() bytes for the
+ *                splits used (unused when 1 split is used); contents on entry do not matter.
+ * Same outputs and errors as fa_fwd; FA_ERR_WORKSPACE if the workspace is too small.
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int num_splits);
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int Hq, int Hkv, int N, int d, int causal, float scale, int num_splits,
+                   void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Same as fa_fwd, and additionally adds to counters[0..2] (device pointer to three
  * unsigned 64-bit integers, which the caller zeroes): [0] key/value tiles computed,
  * [1] key/value tiles skipped by the causal rule, [2] query rows whose running max was

@@ -130,8 +130,27 @@ WorkspaceLayout workspace_layout(int B, int Hq, int N, int d) {
     if (_r != FA_OK) return _r; \
   } while (0)
 
+// Split-KV workspace: fp32 partial outputs [splits][B*Hq][N][d], then partial LSE [splits][B*Hq][N].
+size_t splitkv_bytes(int B, int Hq, int N, int d, int splits, size_t* lse_off) {
+  const size_t rows = (size_t)splits * B * Hq * N;
+  const size_t o_bytes = (rows * d * 4 + 255) / 256 * 256;
+  if (lse_off) *lse_off = o_bytes;
+  return o_bytes + (rows * 4 + 255) / 256 * 256;
+}
+
+// Splits used when the caller asks for automatic selection: enough work items to give every SM
+// one (counting the longest pair), at most 16, and at least 2 key tiles per split.
+int auto_splits(int B, int Hq, int N, int num_sms) {
+  const int T = (N + fa::kTile - 1) / fa::kTile;
+  const long long items = (long long)((T + 1) / 2) * B * Hq;
+  int s = 1;
+  while (s < 16 && items * s < num_sms && T / (2 * s) >= 2) s *= 2;
+  return s;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
-             int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
+             int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream, int window = 0,
+             int num_splits = 1, float* o_part = nullptr, float* lse_part = nullptr) {
   FA_TRY(check_sizes(B, Hq, Hkv, N, d));
   FA_TRY(check_ptr(q));
   FA_TRY(check_ptr(k));
@@ -161,6 +180,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.N = N;
   a.d = d;
   a.causal = causal ? 1 : 0;
+  a.window = window;
+  a.num_splits = num_splits;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
   a.num_sms = num_sms;
   a.scale = resolve_scale(scale, d);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -235,6 +258,39 @@ int fa_fwd_stats(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
   if (counters == nullptr) return FA_ERR_INVALID;
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, counters, stream);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                  int d, int window, float scale, fa_stream_t stream) {
+  if (window < 1) return FA_ERR_INVALID;
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, 1, scale, nullptr, stream, window);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int num_splits) {
+  if (check_sizes(B, Hq, Hkv, N, d) != FA_OK || num_splits < 1 || num_splits > 64) return 0;
+  return splitkv_bytes(B, Hq, N, d, num_splits, nullptr);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
+                   int d, int causal, float scale, int num_splits, void* workspace, size_t workspace_bytes,
+                   fa_stream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  if (num_splits > 64) return FA_ERR_INVALID;
+  if (num_splits <= 0) {
+    int sms = 0;
+    FA_TRY(current_device(nullptr, &sms));
+    num_splits = auto_splits(B, Hq, N, sms);
+  }
+  size_t lse_off = 0;
+  const size_t need = splitkv_bytes(B, Hq, N, d, num_splits, &lse_off);
+  if (num_splits > 1) {
+    if (workspace == nullptr || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
+  }
+  char* ws = static_cast<char*>(workspace);
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream, 0, num_splits,
+                  num_splits > 1 ? reinterpret_cast<float*>(ws) : nullptr,
+                  num_splits > 1 ? reinterpret_cast<float*>(ws + lse_off) : nullptr);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {

@@ -33,21 +33,31 @@ namespace fa {
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
+  float* o_part;    // split-KV partial outputs [num_splits][B*Hq][N][D] fp32 (split mode only)
+  float* lse_part;  // split-KV partial LSE (natural log) [num_splits][B*Hq][N] (split mode only)
   unsigned long long* counters;
   uint32_t* status;
   int B, Hq, Hkv, N, causal;
+  int window;        // > 0: key j visible to query i only if i - window < j (causal as well)
   int num_tiles;     // ceil(N / 128): query tiles per head == key tiles per head
-  int num_pairs;     // ceil(num_tiles / 2): work items per head
-  int num_items;     // num_pairs * B * Hq
+  int num_pairs;     // ceil(num_tiles / 2): query-tile pairs per head
+  int num_splits;    // key-tile ranges per pair (1 = no split)
+  int split_len;     // key tiles per split
+  int num_items;     // num_pairs * B * Hq * num_splits
   float scale_log2;  // scale * log2(e)
 };
 
-// One work item: query tiles 2*pair and 2*pair+1 of head bh. Items are numbered so that, for
-// causal attention, the longest come first (item k -> pair num_pairs-1-k/BH).
+// One work item: query tiles 2*pair and 2*pair+1 of head bh over one range of key tiles. Query
+// tile t visits key tiles [j0 + a[t], j0 + b[t]) (none when a[t] == b[t]): causal tiles stop at
+// the diagonal, a sliding window starts at the first key tile any row of the tile can see, and
+// a split keeps one of num_splits consecutive ranges of split_len key tiles. Items are
+// numbered so that, for causal attention, the longest pairs come first.
 struct FwdItem {
-  int bh, kv_z, qt0, n0, n1, n_max;
-  bool has1;
+  int bh, kv_z, qt0, j0, n_max, split;
+  int a[2], b[2];
+  bool exists[2];  // the query tile has rows (qt < num_tiles)
 };
+
 // Item of this CTA in round r: items are dealt in rounds of gridDim.x, snake order (CTA c gets
 // item r*G + c in even rounds and r*G + G-1-c in odd rounds), which balances the linearly
 // decreasing causal item lengths across CTAs. Returns -1 past the end.
@@ -57,20 +67,49 @@ __device__ __forceinline__ int fwd_item_index(int r, int num_items) {
   return k < num_items ? k : -1;
 }
 
+template <bool kWin, bool kSplit>
 __device__ __forceinline__ FwdItem fwd_item(int k, const FwdParams& p) {
   FwdItem it;
   const int BH = p.B * p.Hq;
-  const int rank = k / BH;
-  it.bh = k - rank * BH;
+  it.split = kSplit ? k % p.num_splits : 0;
+  const int kk = kSplit ? k / p.num_splits : k;
+  const int rank = kk / BH;
+  it.bh = kk - rank * BH;
   const int pair = p.causal ? (p.num_pairs - 1 - rank) : rank;
   const int b = it.bh / p.Hq;
   const int hq = it.bh - b * p.Hq;
   it.kv_z = b * p.Hkv + hq / (p.Hq / p.Hkv);
   it.qt0 = 2 * pair;
-  it.has1 = it.qt0 + 1 < p.num_tiles;
-  it.n0 = p.causal ? (it.qt0 + 1) : p.num_tiles;  // key tiles each query tile visits
-  it.n1 = it.has1 ? (p.causal ? (it.qt0 + 2) : p.num_tiles) : 0;
-  it.n_max = it.has1 ? it.n1 : it.n0;
+  int lo[2], hi[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = it.qt0 + t;
+    it.exists[t] = qt < p.num_tiles;
+    lo[t] = hi[t] = 0;
+    if (!it.exists[t]) continue;
+    hi[t] = p.causal ? qt + 1 : p.num_tiles;
+    lo[t] = kWin ? max(0, qt * kTile - p.window + 1) / kTile : 0;
+    if (kSplit) {
+      lo[t] = max(lo[t], it.split * p.split_len);
+      hi[t] = min(hi[t], (it.split + 1) * p.split_len);
+    }
+    if (hi[t] < lo[t]) hi[t] = lo[t];
+  }
+  it.j0 = 0;
+  bool any = false;
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    if (hi[t] > lo[t]) {
+      it.j0 = any ? min(it.j0, lo[t]) : lo[t];
+      any = true;
+    }
+  it.n_max = 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.a[t] = (hi[t] > lo[t]) ? lo[t] - it.j0 : 0;
+    it.b[t] = (hi[t] > lo[t]) ? hi[t] - it.j0 : 0;
+    it.n_max = max(it.n_max, it.b[t]);
+  }
   return it;
 }
 
@@ -117,14 +156,14 @@ __device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (
   return max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), max3f(m[6], m[7], init));
 }
 
-// Columns past `lim` (the last visible key of this row within the tile) become -inf.
-__device__ __forceinline__ void mask32(uint32_t (&s)[32], int col0, int lim) {
+// Columns outside [lo, lim] (the visible keys of this row within the tile) become -inf.
+__device__ __forceinline__ void mask32(uint32_t (&s)[32], int col0, int lo, int lim) {
 #pragma unroll
   for (int i = 0; i < 32; ++i)
-    if (col0 + i > lim) s[i] = kNegInf;
+    if (col0 + i > lim || col0 + i < lo) s[i] = kNegInf;
 }
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, bool kWin, bool kSplit>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -191,8 +230,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
         const int k = fwd_item_index(r, p.num_items);
         if (k < 0) continue;
-        const FwdItem it = fwd_item(k, p);
-        for (int t = 0; t < (it.has1 ? 2 : 1); ++t) {
+        const FwdItem it = fwd_item<kWin, kSplit>(k, p);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (it.b[t] == it.a[t]) continue;
           if (!(ok = mbar_wait(bar(L::bQEmpty + t), (qn[t] & 1) ^ 1, ctl))) break;
           mbar_expect_tx(bar(L::bQ + t), kBytes);
 #pragma unroll
@@ -202,17 +243,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int j = 0; ok && j < it.n_max; ++j) {
           const uint32_t sk = gk % NK, sv = gv % NV;
+          const int jy = (it.j0 + j) * kTile;
           if (!(ok = mbar_wait(bar(L::bKEmpty + sk), ((gk / NK) & 1) ^ 1, ctl))) break;
           mbar_expect_tx(bar(L::bKFull + sk), kBytes);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sK + sk * kBytes + c * 16384, &tm_k, bar(L::bKFull + sk), c * 64, j * kTile, it.kv_z);
+            tma_load_3d(sK + sk * kBytes + c * 16384, &tm_k, bar(L::bKFull + sk), c * 64, jy, it.kv_z);
           ++gk;
           if (!(ok = mbar_wait(bar(L::bVEmpty + sv), ((gv / NV) & 1) ^ 1, ctl))) break;
           mbar_expect_tx(bar(L::bVFull + sv), kBytes);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(sV + sv * kBytes + c * 16384, &tm_v, bar(L::bVFull + sv), c * 64, j * kTile, it.kv_z);
+            tma_load_3d(sV + sv * kBytes + c * 16384, &tm_v, bar(L::bVFull + sv), c * 64, jy, it.kv_z);
           ++gv;
         }
       }
@@ -229,7 +271,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
       uint32_t gk = 0, gv = 0;  // K and V tiles consumed so far
-      uint32_t qn[2] = {0, 0};  // items that used query tile t
+      uint32_t qn[2] = {0, 0};  // items in which query tile t was active
       uint32_t pc[2] = {0, 0};  // P.V MMAs issued for tile t
       auto issue_s = [&](int t, uint32_t g) -> bool {  // S_t = Q_t K^T with K tile number g
         const uint32_t sk = g % NK;
@@ -269,31 +311,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
         const int k = fwd_item_index(r, p.num_items);
         if (k < 0) continue;
-        const FwdItem it = fwd_item(k, p);
-        for (int t = 0; ok && t < (it.has1 ? 2 : 1); ++t) {
+        const FwdItem it = fwd_item<kWin, kSplit>(k, p);
+        if (it.n_max == 0) continue;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (it.b[t] == it.a[t]) continue;
           if (!(ok = mbar_wait(bar(L::bQ + t), qn[t] & 1, ctl))) break;
           ++qn[t];
           tc_fence_after();
-          if (!(ok = issue_s(t, gk))) break;
-          if ((t ? it.n1 : it.n0) == 1) mma_commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
+          if (it.a[t] == 0) {  // score MMA of the item's first key tile
+            if (!(ok = issue_s(t, gk))) break;
+            if (it.b[t] == 1) mma_commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
+          }
         }
         if (!ok) break;
-        mma_commit(bar(L::bKEmpty + gk % NK));  // K tile 0 of the item: both score MMAs issued
+        mma_commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
         for (int j = 0; ok && j < it.n_max; ++j) {
-          if (j < it.n0) {
-            if (!(ok = issue_pv(0, gv + j, j == 0))) break;
-            if (j + 1 < it.n0) {
-              if (!(ok = issue_s(0, gk + j + 1))) break;
-              if (j + 2 == it.n0) mma_commit(bar(L::bQEmpty));
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (it.a[t] <= j && j < it.b[t] && !(ok = issue_pv(t, gv + j, j == it.a[t]))) break;
+            if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
+              if (!(ok = issue_s(t, gk + j + 1))) break;
+              if (j + 2 == it.b[t]) mma_commit(bar(L::bQEmpty + t));
             }
           }
-          if (j < it.n1) {
-            if (!(ok = issue_pv(1, gv + j, j == 0))) break;
-            if (j + 1 < it.n1) {
-              if (!(ok = issue_s(1, gk + j + 1))) break;
-              if (j + 2 == it.n1) mma_commit(bar(L::bQEmpty + 1));
-            }
-          }
+          if (!ok) break;
           mma_commit(bar(L::bVEmpty + (gv + j) % NV));
           if (j + 1 < it.n_max) mma_commit(bar(L::bKEmpty + (gk + j + 1) % NK));
         }
@@ -315,13 +358,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t sc = 0;  // score tiles of this query tile processed so far (all items)
     bool ok = true;
     for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
-        const int k = fwd_item_index(r, p.num_items);
-        if (k < 0) continue;
-      const FwdItem itm = fwd_item(k, p);
-      const int n_kv = t ? itm.n1 : itm.n0;
-      if (n_kv == 0) continue;
+      const int k = fwd_item_index(r, p.num_items);
+      if (k < 0) continue;
+      const FwdItem itm = fwd_item<kWin, kSplit>(k, p);
+      if (!(t ? itm.exists[1] : itm.exists[0])) continue;
       const int qt = itm.qt0 + t;
       const int row = qt * kTile + (threadIdx.x & 127);
+      const int a_t = t ? itm.a[1] : itm.a[0];
+      const int n_kv = (t ? itm.b[1] : itm.b[0]) - a_t;
+      const size_t part_row = ((size_t)itm.split * p.B * p.Hq + itm.bh) * p.N + row;
+      if (n_kv == 0) {
+        // This split has no key tile for this query tile: an empty partial (weight zero).
+        if (kSplit && row < p.N) {
+          p.lse_part[part_row] = -INFINITY;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + part_row * D);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      const int jbase = itm.j0 + a_t;  // absolute index of the first key tile
       float m_run = -INFINITY;
       float l_run = 0.f;
       uint32_t n_rescaled = 0;
@@ -331,9 +387,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           break;
         }
         tc_fence_after();
-        const int kv0 = j * kTile;
-        const bool need_mask = (p.causal && j == qt) || kv0 + kTile > p.N;
-        const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;  // last visible column
+        const int kv0 = (jbase + j) * kTile;
+        // Visible columns of this row within the tile: [lo, lim].
+        const bool need_mask = (p.causal && jbase + j == qt) || kv0 + kTile > p.N ||
+                               (kWin && kv0 < qt * kTile + kTile - p.window);
+        const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;
+        const int lo = kWin ? row - p.window + 1 - kv0 : -kTile;
         // Pass 1: row max.
         float mx = -INFINITY;
 #pragma unroll
@@ -344,8 +403,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_ld_wait(a);
           tmem_ld_wait(b2);
           if (need_mask) {
-            mask32(a, c * 32, lim);
-            mask32(b2, (c + 1) * 32, lim);
+            mask32(a, c * 32, lo, lim);
+            mask32(b2, (c + 1) * 32, lo, lim);
           }
           mx = max64(a, b2, mx);
         }
@@ -389,7 +448,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           uint32_t a[32];
           tmem_ld32(tS + c * 32, a);
           tmem_ld_wait(a);
-          if (need_mask) mask32(a, c * 32, lim);
+          if (need_mask) mask32(a, c * 32, lo, lim);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -412,6 +471,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       sc += n_kv;
       tc_fence_after();
       const float inv_l = 1.f / l_run;
+      if (kSplit) {
+        // Split mode: the partial output acc / l (fp32) and its LSE, merged later.
+        if (row < p.N) p.lse_part[part_row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
+        float4* dst = reinterpret_cast<float4*>(p.o_part + part_row * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          if (row < p.N) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                           __uint_as_float(o[4 * i + 2]) * inv_l,
+                                           __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(L::bOFree + t));
+        continue;
+      }
       uint4 w[D / 32][4];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -437,7 +517,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < 4; ++i) dst[c * 4 + i] = w[c][i];
         p.lse[(size_t)itm.bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
       }
-      if (p.counters != nullptr) {
+      if (!kSplit && p.counters != nullptr) {
         unsigned int r = n_rescaled;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
@@ -459,22 +539,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, int NK, int NV>
-static cudaError_t launch_fwd_t(const FwdLaunch& a, const FwdParams& p) {
+template <int D, int NK, int NV, bool kWin, bool kSplit>
+static cudaError_t launch_fwd_mode(const FwdLaunch& a, const FwdParams& p) {
   constexpr int smem = FwdSmem<D, NK, NV>::kAlloc;
   static_assert(smem <= 232448, "forward shared memory exceeds the 227 KB per-CTA limit");
-  cudaError_t e =
-      cudaFuncSetAttribute(fa_fwd_kernel<D, NK, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, NK, NV, kWin, kSplit>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
-  fa_fwd_kernel<D, NK, NV><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+  fa_fwd_kernel<D, NK, NV, kWin, kSplit><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
   return cudaGetLastError();
+}
+
+// Plain, sliding-window and split-KV forwards are separate instantiations, so the plain kernel
+// carries none of the other modes' index arithmetic.
+template <int D, int NK, int NV>
+static cudaError_t launch_fwd_t(const FwdLaunch& a, const FwdParams& p) {
+  if (p.num_splits > 1) return launch_fwd_mode<D, NK, NV, false, true>(a, p);
+  if (p.window > 0) return launch_fwd_mode<D, NK, NV, true, false>(a, p);
+  return launch_fwd_mode<D, NK, NV, false, false>(a, p);
+}
+
+// Split-KV merge ("LLM Architecture Refresh [3]", section 3, "Partial softmaxes compose"): per
+// row, O = sum_s w_s O_s / sum_s w_s and LSE = m + ln(sum_s w_s) with w_s = exp(LSE_s - m),
+// m = max_s LSE_s. One thread per 4 columns of a row.
+template <int D>
+__global__ void __launch_bounds__(256) fa_split_merge_kernel(const float* __restrict__ o_part,
+                                                            const float* __restrict__ lse_part,
+                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                            long long rows, int num_splits) {
+  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gt / (D / 4);
+  const int col = (int)(gt - row * (D / 4)) * 4;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + row]);
+  float wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < num_splits; ++s) {
+    const float ls = lse_part[(size_t)s * rows + row];
+    if (ls == -INFINITY) continue;  // empty partial
+    const float w = __expf(ls - m);
+    const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)s * rows + row) * D + col);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+    wsum += w;
+  }
+  const float inv = 1.f / wsum;
+  uint2 packed;
+  packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(o + row * D + col) = packed;
+  if (col == 0) lse[row] = m + __logf(wsum);
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a) {
   FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.window = a.window;
   p.counters = a.counters;
   p.status = a.status;
   p.B = a.B;
@@ -484,10 +611,20 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.causal = a.causal;
   p.num_tiles = (a.N + kTile - 1) / kTile;
   p.num_pairs = (p.num_tiles + 1) / 2;
-  p.num_items = p.num_pairs * a.B * a.Hq;
+  p.num_splits = a.num_splits > 1 ? a.num_splits : 1;
+  p.split_len = (p.num_tiles + p.num_splits - 1) / p.num_splits;
+  p.num_items = p.num_pairs * a.B * a.Hq * p.num_splits;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (a.d == 128) return launch_fwd_t<128, 3, 2>(a, p);
-  return launch_fwd_t<64, 4, 4>(a, p);
+  cudaError_t e = (a.d == 128) ? launch_fwd_t<128, 3, 2>(a, p) : launch_fwd_t<64, 4, 4>(a, p);
+  if (e != cudaSuccess || p.num_splits == 1) return e;
+  const long long rows = (long long)a.B * a.Hq * a.N;
+  const long long threads = rows * (a.d / 4);
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (a.d == 128)
+    fa_split_merge_kernel<128><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p.num_splits);
+  else
+    fa_split_merge_kernel<64><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p.num_splits);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -18,7 +18,11 @@ struct FwdLaunch {
   unsigned long long* counters;  // nullable
   uint32_t* status;
   int B, Hq, Hkv, N, d, causal;
-  int num_sms;  // persistent grid size
+  int window;      // 0: none; > 0: causal sliding window of this many keys
+  int num_splits;  // 1: plain; > 1: split-KV into o_part / lse_part, then merged into o / lse
+  float* o_part;   // [num_splits][B*Hq][N][d] fp32 (split mode)
+  float* lse_part; // [num_splits][B*Hq][N] fp32 (split mode)
+  int num_sms;     // persistent grid size
   float scale;
   cudaStream_t stream;
 };

@@ -52,6 +52,13 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_compute.restype = _i
         L.fa_bwd_finalize.argtypes = [_vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd_finalize.restype = _i
+        L.fa_fwd_window.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_fwd_window.restype = _i
+        L.fa_fwd_splitkv_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
+        L.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_fwd_splitkv.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
+                                     ctypes.c_size_t, _vp]
+        L.fa_fwd_splitkv.restype = _i
         L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]
         L.fa_softmax_rows.restype = _i
         L.fa_check.argtypes = [_vp]
@@ -99,6 +106,37 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                                B, Hq, Hkv, N, d, int(bool(causal)), sc, counters.data_ptr(), h)
     if r != FA_OK:
         raise FAError(r, "fa_fwd")
+    return o, l
+
+
+def forward_window(q, k, v, window: int, scale: float | None = None, out=None, lse=None, stream=None):
+    """Causal sliding-window attention (fa_fwd_window): query i sees keys i-window < j <= i."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                            B, Hq, Hkv, N, d, int(window), sc, _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_fwd_window")
+    return o, l
+
+
+def forward_splitkv(q, k, v, causal: bool = False, num_splits: int = 0, scale: float | None = None,
+                    out=None, lse=None, workspace=None, stream=None):
+    """Split-KV forward (fa_fwd_splitkv); num_splits <= 0 lets the library choose."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = int(lib().fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, N, d, int(num_splits) if num_splits > 0 else 16))
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                             B, Hq, Hkv, N, d, int(bool(causal)), sc, int(num_splits), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_fwd_splitkv")
     return o, l
 
 

@@ -36,6 +36,7 @@ from .attention import (  # noqa: F401
     attention_probs,
     attention_query_block,
     attention_rows,
+    attention_split_forward_head,
     brute_force_attention,
     causal_tile_counts,
     naive_counts,

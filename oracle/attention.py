@@ -48,21 +48,36 @@ def _causal_mask(n_q: int, n_k: int, q_start: int = 0, k_start: int = 0) -> np.n
     return kj > qi
 
 
-def attention_probs(q: np.ndarray, k: np.ndarray, causal: bool, scale: float) -> np.ndarray:
+def _masked(n_q: int, n_k: int, causal: bool, window=None, q_start: int = 0, k_start: int = 0):
+    """True where a key is invisible to a query: in the future (causal), or, with a sliding
+    window of w keys, older than the w most recent ones: key < query - w + 1 ([P3] section 5,
+    sliding_window_attention's too_old mask, which is causal as well). None: nothing masked."""
+    mask = None
+    if causal or window is not None:
+        mask = _causal_mask(n_q, n_k, q_start, k_start)
+    if window is not None:
+        qi = np.arange(q_start, q_start + n_q)[:, None]
+        kj = np.arange(k_start, k_start + n_k)[None, :]
+        mask = mask | (kj < qi - window + 1)
+    return mask
+
+
+def attention_probs(q: np.ndarray, k: np.ndarray, causal: bool, scale: float, window=None) -> np.ndarray:
     """Row-softmax weights P for ONE head: q [N,d], k [N,d] -> P [N,N].
 
     Numerically stable softmax with the row max subtracted ([P3] section 2,
     [P1] "The Running Statistics"): ``P_ij = exp(S_ij - m_i) / sum_j exp(S_ij - m_i)``.
     """
     S = scale * (q @ k.T)
-    if causal:
-        S = np.where(_causal_mask(q.shape[0], k.shape[0]), -np.inf, S)
+    mask = _masked(q.shape[0], k.shape[0], causal, window)
+    if mask is not None:
+        S = np.where(mask, -np.inf, S)
     m = S.max(axis=1, keepdims=True)
     P = np.exp(S - m)
     return P / P.sum(axis=1, keepdims=True)
 
 
-def attention_forward_head(q, k, v, causal: bool, scale: float):
+def attention_forward_head(q, k, v, causal: bool, scale: float, window=None):
     """Standard attention for one head, fully materialised ([P3] section 1).
 
     ``S = scale * Q K^T``; masked if causal; ``m = rowmax(S)``;
@@ -73,8 +88,9 @@ def attention_forward_head(q, k, v, causal: bool, scale: float):
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     S = scale * (q @ k.T)
-    if causal:
-        S = np.where(_causal_mask(q.shape[0], k.shape[0]), -np.inf, S)
+    mask = _masked(q.shape[0], k.shape[0], causal, window)
+    if mask is not None:
+        S = np.where(mask, -np.inf, S)
     m = S.max(axis=1, keepdims=True)
     P = np.exp(S - m)
     l = P.sum(axis=1, keepdims=True)
@@ -83,7 +99,7 @@ def attention_forward_head(q, k, v, causal: bool, scale: float):
     return O, lse
 
 
-def attention_forward(q, k, v, causal: bool, scale: float):
+def attention_forward(q, k, v, causal: bool, scale: float, window=None):
     """Standard attention over ``[B,Hq,N,d]`` / ``[B,Hkv,N,d]`` arrays.
 
     Head by head (to bound memory); returns ``(O [B,Hq,N,d], LSE [B,Hq,N])``.
@@ -95,11 +111,11 @@ def attention_forward(q, k, v, causal: bool, scale: float):
     for b in range(B):
         for h in range(Hq):
             hk = _kv_head(h, Hq, Hkv)
-            O[b, h], lse[b, h] = attention_forward_head(q[b, h], k[b, hk], v[b, hk], causal, scale)
+            O[b, h], lse[b, h] = attention_forward_head(q[b, h], k[b, hk], v[b, hk], causal, scale, window)
     return O, lse
 
 
-def attention_rows(q_rows, k, v, rows, causal: bool, scale: float):
+def attention_rows(q_rows, k, v, rows, causal: bool, scale: float, window=None):
     """Standard attention for SELECTED query rows of one head.
 
     ``q_rows`` [R,d] holds the queries at absolute positions ``rows`` (for the
@@ -111,8 +127,10 @@ def attention_rows(q_rows, k, v, rows, causal: bool, scale: float):
     v = np.asarray(v, dtype=np.float64)
     rows = np.asarray(rows)
     S = scale * (q_rows @ k.T)
-    if causal:
+    if causal or window is not None:
         S = np.where(np.arange(k.shape[0])[None, :] > rows[:, None], -np.inf, S)
+    if window is not None:
+        S = np.where(np.arange(k.shape[0])[None, :] < rows[:, None] - window + 1, -np.inf, S)
     m = S.max(axis=1, keepdims=True)
     P = np.exp(S - m)
     l = P.sum(axis=1, keepdims=True)
@@ -124,7 +142,7 @@ def attention_rows(q_rows, k, v, rows, causal: bool, scale: float):
 # --------------------------------------------------------------------------
 
 
-def attention_backward_head(q, k, v, do, causal: bool, scale: float):
+def attention_backward_head(q, k, v, do, causal: bool, scale: float, window=None):
     """Gradients of standard attention for one head.
 
     [P3] section 8 ("One more piece: the backward pass") says only that the
@@ -138,7 +156,7 @@ def attention_backward_head(q, k, v, do, causal: bool, scale: float):
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     do = np.asarray(do, dtype=np.float64)
-    P = attention_probs(q, k, causal, scale)
+    P = attention_probs(q, k, causal, scale, window)
     O = P @ v
     dV = P.T @ do
     dP = do @ v.T
@@ -149,7 +167,7 @@ def attention_backward_head(q, k, v, do, causal: bool, scale: float):
     return dQ, dK, dV
 
 
-def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):
+def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None, window=None):
     """Gradients over ``[B,Hq,N,d]`` arrays; dK, dV summed over each GQA group.
 
     ``heads`` optionally restricts the computation to a list of ``(b, hkv)``
@@ -167,7 +185,7 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):
         dk[b, hk] = 0.0
         dv[b, hk] = 0.0
         for hq in range(hk * G, (hk + 1) * G):
-            gq, gk, gv = attention_backward_head(q[b, hq], k[b, hk], v[b, hk], do[b, hq], causal, scale)
+            gq, gk, gv = attention_backward_head(q[b, hq], k[b, hk], v[b, hk], do[b, hq], causal, scale, window)
             dq[b, hq] = gq
             dk[b, hk] += gk
             dv[b, hk] += gv
@@ -179,7 +197,7 @@ def attention_backward(q, k, v, do, causal: bool, scale: float, heads=None):
 # --------------------------------------------------------------------------
 
 
-def brute_force_attention(q, k, v, causal: bool, scale: float):
+def brute_force_attention(q, k, v, causal: bool, scale: float, window=None):
     """Softmax attention by explicit scalar loops (one head, small N only).
 
     Written straight from the softmax definition of [P1] ("Here's the
@@ -190,7 +208,9 @@ def brute_force_attention(q, k, v, causal: bool, scale: float):
     dv = len(v[0])
     O, lse = [], []
     for i in range(N):
-        keys = range(i + 1) if causal else range(N)
+        keys = range(i + 1) if (causal or window is not None) else range(N)
+        if window is not None:
+            keys = range(max(0, i - window + 1), i + 1)
         s = {}
         for j in keys:
             acc = 0.0
@@ -441,3 +461,34 @@ def attention_query_block(q, k, v, do, rows, causal: bool, scale: float):
     dK = scale * (dS.T @ q[rows])
     dV = P.T @ do[rows]
     return O, m[:, 0] + np.log(l[:, 0]), dQ, dK, dV
+
+
+def attention_split_forward_head(q, k, v, causal: bool, scale: float, splits: int):
+    """Forward of one head computed as `splits` partial softmaxes over contiguous key ranges,
+    then merged ([P3] section 3, "Partial softmaxes compose"): each range gives a partial
+    output O_s (normalised over its own keys) and LSE_s (minus infinity when a row sees none
+    of its keys); with m = max_s LSE_s and w_s = exp(LSE_s - m),
+    O = sum_s w_s O_s / sum_s w_s and LSE = m + ln(sum_s w_s)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    N = k.shape[0]
+    bounds = np.linspace(0, N, splits + 1).astype(int)
+    parts = []
+    for s0, s1 in zip(bounds[:-1], bounds[1:]):
+        S = scale * (q @ k[s0:s1].T)
+        if causal:
+            S = np.where(_causal_mask(q.shape[0], s1 - s0, 0, s0), -np.inf, S)
+        m = S.max(axis=1, keepdims=True) if s1 > s0 else np.full((q.shape[0], 1), -np.inf)
+        with np.errstate(invalid="ignore"):
+            P = np.exp(S - np.where(np.isneginf(m), 0.0, m))
+        l = P.sum(axis=1, keepdims=True)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            O_s = np.where(l > 0, (P @ v[s0:s1]) / np.where(l > 0, l, 1.0), 0.0)
+            lse_s = np.where(l[:, 0] > 0, m[:, 0] + np.log(np.where(l[:, 0] > 0, l[:, 0], 1.0)), -np.inf)
+        parts.append((O_s, lse_s))
+    m = np.max([ls for _, ls in parts], axis=0)
+    w = [np.exp(ls - m) for _, ls in parts]
+    wsum = np.sum(w, axis=0)
+    O = sum(wi[:, None] * Oi for wi, (Oi, _) in zip(w, parts)) / wsum[:, None]
+    return O, m + np.log(wsum)

@@ -343,3 +343,77 @@ def test_query_blocks_sum_to_full_backward(causal):
         sv += vb
     np.testing.assert_allclose(sk, dk, atol=1e-12)
     np.testing.assert_allclose(sv, dv, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Sliding window ([P3] section 5) and split-then-merge ([P3] section 3).
+# ---------------------------------------------------------------------------
+
+
+def test_window_at_least_n_equals_causal():
+    rng = _rng(31)
+    q, k, v = (rng.standard_normal((40, 6)) for _ in range(3))
+    for w in (40, 41, 1000):
+        O, L = oracle.attention_forward_head(q, k, v, False, 0.5, window=w)
+        Oc, Lc = oracle.attention_forward_head(q, k, v, True, 0.5)
+        np.testing.assert_allclose(O, Oc, atol=1e-14)
+        np.testing.assert_allclose(L, Lc, atol=1e-14)
+
+
+def test_window_of_one_sees_only_itself():
+    rng = _rng(32)
+    q, k, v = (rng.standard_normal((17, 5)) for _ in range(3))
+    O, L = oracle.attention_forward_head(q, k, v, False, 0.5, window=1)
+    np.testing.assert_allclose(O, v, atol=1e-14)
+    np.testing.assert_allclose(L, 0.5 * np.sum(q * k, axis=1), atol=1e-14)
+
+
+@pytest.mark.parametrize("w", [1, 2, 3, 5])
+def test_window_brute_force(w):
+    rng = _rng(33 + w)
+    q, k, v = (rng.standard_normal((7, 3)) for _ in range(3))
+    O, L = oracle.attention_forward_head(q, k, v, False, 0.6, window=w)
+    Ob, Lb = oracle.brute_force_attention(q.tolist(), k.tolist(), v.tolist(), False, 0.6, window=w)
+    np.testing.assert_allclose(O, np.array(Ob), atol=1e-12)
+    np.testing.assert_allclose(L, np.array(Lb), atol=1e-12)
+    rows = np.array([0, 3, 6])
+    Or, Lr = oracle.attention_rows(q[rows], k, v, rows, False, 0.6, window=w)
+    np.testing.assert_allclose(Or, O[rows], atol=1e-13)
+    np.testing.assert_allclose(Lr, L[rows], atol=1e-13)
+
+
+def test_window_backward_finite_differences():
+    rng = _rng(34)
+    B, Hq, Hkv, N, d, w = 1, 2, 1, 6, 3, 3
+    q = rng.standard_normal((B, Hq, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    do = rng.standard_normal((B, Hq, N, d))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, True, 0.5, window=w)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            args = {"q": q, "k": k, "v": v}
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args[name] = xp
+            lp = float(np.sum(oracle.attention_forward(args["q"], args["k"], args["v"], True, 0.5, window=w)[0] * do))
+            args[name] = xm
+            lm = float(np.sum(oracle.attention_forward(args["q"], args["k"], args["v"], True, 0.5, window=w)[0] * do))
+            num[idx] = (lp - lm) / (2 * h)
+        assert np.linalg.norm(g - num) / np.linalg.norm(num) < 1e-7, name
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 50])
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_then_merge_equals_full(splits, causal):
+    rng = _rng(35)
+    q, k, v = (rng.standard_normal((50, 4)) * 2 for _ in range(3))
+    O, L = oracle.attention_forward_head(q, k, v, causal, 0.4)
+    Os, Ls = oracle.attention_split_forward_head(q, k, v, causal, 0.4, splits)
+    np.testing.assert_allclose(Os, O, atol=1e-12)
+    np.testing.assert_allclose(Ls, L, atol=1e-12)
