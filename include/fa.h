@@ -131,6 +131,17 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const voi
            fa_stream_t stream);
 
 /*
+ * Backward of fa_fwd_window: the same as fa_bwd for the causal sliding window of `window`
+ * keys (query i sees keys i - window < j <= i); query tiles wholly outside a key tile's reach
+ * are skipped. window >= 1; workspace as for fa_bwd.
+ */
+int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                  const float *lse, void *dq, void *dk, void *dv,
+                  void *workspace, size_t workspace_bytes,
+                  int B, int Hq, int Hkv, int N, int d, int window, float scale,
+                  fa_stream_t stream);
+
+/*
  * The three stages fa_bwd runs, exposed so that a caller can schedule or time them apart.
  * They must be called in this order on one stream with the same sizes and workspace;
  * fa_bwd(...) is exactly prepare, compute, finalize.

@@ -192,7 +192,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,
-             int d, int causal, float scale, fa_stream_t stream, int stages) {
+             int d, int causal, float scale, fa_stream_t stream, int stages, int window = 0) {
   FA_TRY(check_sizes(B, Hq, Hkv, N, d));
   // Pointers each stage reads or writes.
   if (stages & fa::kBwdPrepare) {
@@ -239,7 +239,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.Hkv = Hkv;
   a.N = N;
   a.d = d;
-  a.causal = causal ? 1 : 0;
+  a.causal = (causal || window > 0) ? 1 : 0;
+  a.window = window;
   a.scale = resolve_scale(scale, d);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return fa::launch_bwd(a, stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
@@ -303,6 +304,14 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int N, int d, int causal, float scale, fa_stream_t stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale,
                   stream, fa::kBwdAll);
+}
+
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                  int N, int d, int window, float scale, fa_stream_t stream) {
+  if (window < 1) return FA_ERR_INVALID;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, 1, scale,
+                  stream, fa::kBwdAll, window);
 }
 
 int fa_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace, size_t workspace_bytes,

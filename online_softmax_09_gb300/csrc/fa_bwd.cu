@@ -112,6 +112,7 @@ struct BwdParams {
   const float* lse2;
   uint32_t* status;
   int B, Hq, Hkv, N, Npad, causal, num_tiles;
+  int window;  // > 0: causal sliding window of this many keys
   float scale, scale_log2;
 };
 
@@ -158,7 +159,7 @@ struct BwdSmem {
 
 constexpr int kBwdThreads = 320;
 
-template <int D>
+template <int D, bool kWin>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -188,8 +189,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = bhk / p.Hkv;
   const int hkv = bhk - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
-  const int n_i = p.causal ? (p.num_tiles - n) : p.num_tiles;
+  // Query tiles that see key tile n: from the diagonal (causal) to, with a sliding window, the
+  // tile of the last query within `window` of the tile's last key.
   const int i0 = p.causal ? n : 0;
+  const int i_end = kWin ? min(p.num_tiles, (n * kTile + kTile - 1 + p.window - 1) / kTile + 1) : p.num_tiles;
+  const int n_i = i_end - i0;
   const int n_iter = G * n_i;
   auto item = [&](int it, int& hq, int& i) {
     const int g = it / n_i;
@@ -364,6 +368,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int hq, i;
       item(it, hq, i);
       const bool diag = p.causal && i == n;
+      // Window: query q sees key j only if q - j < window; (i - n) * 128 + q - kr is q - j.
+      const bool wmask = kWin && (i - n) * kTile + kTile - 1 >= p.window;
       const float* sl = reinterpret_cast<const float*>(stage_ptr(s) + L::kStL);
       if (!mbar_wait_warp(bar(L::bQFull + s), (it >> 1) & 1, ctl)) return false;
       if (!mbar_wait_warp(bar(L::bSFull), it & 1, ctl)) return false;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int t = 0; t < 4; ++t) {
             const int q = c * 32 + j + t;
             pv[t] = ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
-            if (!key_ok || (diag && q < kr)) pv[t] = 0.f;
+            if (!key_ok || (diag && q < kr) || (wmask && (i - n) * kTile + q - kr >= p.window)) pv[t] = 0.f;
           }
           pk[c][j / 2] = pack_bf16(pv[0], pv[1]);
           pk[c][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -534,7 +540,8 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
   if (stages & kBwdCompute) {
     constexpr int smem = BwdSmem<D>::kAlloc;
     static_assert(smem <= 232448, "backward shared memory exceeds the 227 KB per-CTA limit");
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = a.window > 0 ? fa_bwd_main_kernel<D, true> : fa_bwd_main_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     BwdParams p;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
@@ -550,11 +557,11 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     p.Npad = Npad;
     p.causal = a.causal;
     p.num_tiles = T;
+    p.window = a.window;
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
     const long long grid = (long long)a.B * a.Hkv * T;
-    fa_bwd_main_kernel<D><<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do,
-                                                                          *a.tm_dq, p);
+    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

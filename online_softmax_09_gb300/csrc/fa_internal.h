@@ -45,6 +45,7 @@ struct BwdLaunch {
   float* lse2;     // workspace: [B*Hq][Npad] fp32 (LSE * log2 e; +inf on padded rows)
   uint32_t* status;
   int B, Hq, Hkv, N, d, causal;
+  int window;  // 0: none; > 0: causal sliding window
   float scale;
   cudaStream_t stream;
 };

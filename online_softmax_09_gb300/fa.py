@@ -46,6 +46,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd.restype = _i
+        L.fa_bwd_window.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_bwd_window.restype = _i
         L.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _vp]
         L.fa_bwd_prepare.restype = _i
         L.fa_bwd_compute.argtypes = [_vp] * 7 + [ctypes.c_size_t, _i, _i, _i, _i, _i, _i, _f, _vp]
@@ -162,6 +164,25 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
                      B, Hq, Hkv, N, d, int(bool(causal)), sc, _stream_handle(stream, q.device))
     if r != FA_OK:
         raise FAError(r, "fa_bwd")
+    return dq, dk, dv
+
+
+def backward_window(q, k, v, o, do, lse, window: int, scale: float | None = None,
+                    dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of causal sliding-window attention (fa_bwd_window)."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    ws = workspace if workspace is not None else torch.empty(workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8,
+                                                              device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                            ws.numel() * ws.element_size(), B, Hq, Hkv, N, d, int(window), sc,
+                            _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_bwd_window")
     return dq, dk, dv
 
 

@@ -386,7 +386,8 @@ def algorithmic_flops(B: int, Hq: int, N: int, d: int, causal: bool) -> int:
     return 4 * d * pairs * B * Hq
 
 
-def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: float, chunk: int = 1024):
+def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: float, chunk: int = 1024,
+                            window=None):
     """Backward of standard attention for ONE head, on selected rows only.
 
     Returns ``(dQ[q_rows], dK[k_rows], dV[k_rows])`` without forming the N x N matrices:
@@ -405,14 +406,16 @@ def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: fl
     delta = np.empty(N)
     for s in range(0, N, chunk):
         rows = np.arange(s, min(N, s + chunk))
-        O_c, lse[rows] = attention_rows(q[rows], k, v, rows, causal, scale)
+        O_c, lse[rows] = attention_rows(q[rows], k, v, rows, causal, scale, window)
         delta[rows] = np.sum(do[rows] * O_c, axis=1)
     q_rows = np.asarray(q_rows)
     k_rows = np.asarray(k_rows)
     # dQ for the selected queries.
     S = scale * (q[q_rows] @ k.T)
-    if causal:
+    if causal or window is not None:
         S = np.where(np.arange(N)[None, :] > q_rows[:, None], -np.inf, S)
+    if window is not None:
+        S = np.where(np.arange(N)[None, :] < q_rows[:, None] - window + 1, -np.inf, S)
     P = np.exp(S - lse[q_rows, None])
     dS = P * (do[q_rows] @ v.T - delta[q_rows, None])
     dQ = scale * (dS @ k)
@@ -422,8 +425,10 @@ def attention_backward_rows(q, k, v, do, q_rows, k_rows, causal: bool, scale: fl
     for s in range(0, N, chunk):
         rows = np.arange(s, min(N, s + chunk))
         St = scale * (q[rows] @ k[k_rows].T)
-        if causal:
+        if causal or window is not None:
             St = np.where(k_rows[None, :] > rows[:, None], -np.inf, St)
+        if window is not None:
+            St = np.where(k_rows[None, :] < rows[:, None] - window + 1, -np.inf, St)
         Pt = np.exp(St - lse[rows, None])
         dSt = Pt * (do[rows] @ v[k_rows].T - delta[rows, None])
         dV += Pt.T @ do[rows]

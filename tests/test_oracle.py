@@ -417,3 +417,15 @@ def test_split_then_merge_equals_full(splits, causal):
     Os, Ls = oracle.attention_split_forward_head(q, k, v, causal, 0.4, splits)
     np.testing.assert_allclose(Os, O, atol=1e-12)
     np.testing.assert_allclose(Ls, L, atol=1e-12)
+
+
+def test_backward_rows_with_window_matches_full():
+    rng = _rng(36)
+    N, d, w = 60, 4, 9
+    q, k, v, do = (rng.standard_normal((N, d)) for _ in range(4))
+    dq, dk, dv = oracle.attention_backward_head(q, k, v, do, True, 0.4, window=w)
+    qr, kr = np.array([0, 8, 9, 59]), np.array([0, 30, 50, 59])
+    rq, rk, rv = oracle.attention_backward_rows(q, k, v, do, qr, kr, True, 0.4, chunk=16, window=w)
+    np.testing.assert_allclose(rq, dq[qr], atol=1e-12)
+    np.testing.assert_allclose(rk, dk[kr], atol=1e-12)
+    np.testing.assert_allclose(rv, dv[kr], atol=1e-12)

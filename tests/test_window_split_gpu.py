@@ -79,3 +79,49 @@ def test_splitkv_auto_and_matches_plain_forward():
     O_ref, L_ref = oracle.attention_forward(to_f64(q), to_f64(k), to_f64(v), True, 1 / math.sqrt(128))
     assert_fwd_close(o_s.float().cpu().numpy(), l_s.cpu().numpy(), O_ref, L_ref, "auto split")
     assert float((o_s.float() - o_p.float()).abs().max()) < 2e-2
+
+
+@pytest.mark.parametrize("N", [7, 300, 1024])
+@pytest.mark.parametrize("window", [1, 5, 129, 300, 5000])
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_backward(N, window, d):
+    from gpu_util import GRAD_REL_TOL, rel_fro
+
+    fa = fa_mod()
+    q, k, v, do = make_qkv(2, 4, 2, N, d, seed=5000 + N + window + d, with_do=True)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.forward_window(qd, kd, vd, window)
+    dq, dk, dv = fa.backward_window(qd, kd, vd, o, dod, lse, window)
+    fa.check()
+    ref = oracle.attention_backward(to_f64(q), to_f64(k), to_f64(v), to_f64(do), True, 1 / math.sqrt(d),
+                                    window=window)
+    floor = 1e-3 * np.linalg.norm(ref[2])
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        e = rel_fro(g.float().cpu().numpy(), r, floor)
+        assert e <= GRAD_REL_TOL, f"{name}: {e:.3e}"
+
+
+def test_window_backward_long_sequence_sampled():
+    from gpu_util import GRAD_REL_TOL, rel_fro
+
+    fa = fa_mod()
+    B, Hq, Hkv, N, d, w = 1, 4, 2, 8192, 128, 1000
+    q, k, v, do = make_qkv(B, Hq, Hkv, N, d, seed=44, value_scale=0.5, with_do=True)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.forward_window(qd, kd, vd, w)
+    dq, dk, dv = fa.backward_window(qd, kd, vd, o, dod, lse, w)
+    fa.check()
+    rows = sample_rows(N, 32, seed=44) + [998, 999, 1000, 1127, 1128]
+    idx = torch.as_tensor(rows, device="cuda")
+    h = 3
+    args = (to_f64(q[0, h]), to_f64(k[0, h // 2]), to_f64(v[0, h // 2]), to_f64(do[0, h]))
+    rq, _, _ = oracle.attention_backward_rows(*args, rows, rows, True, 1 / math.sqrt(d), window=w)
+    assert rel_fro(dq[0, h, idx].float().cpu().numpy(), rq) <= GRAD_REL_TOL
+    # dK, dV of kv head 1 sum over query heads 2 and 3.
+    rk = rv = 0
+    for hq in (2, 3):
+        a = (to_f64(q[0, hq]), to_f64(k[0, 1]), to_f64(v[0, 1]), to_f64(do[0, hq]))
+        _, gk, gv = oracle.attention_backward_rows(*a, rows, rows, True, 1 / math.sqrt(d), window=w)
+        rk, rv = rk + gk, rv + gv
+    assert rel_fro(dk[0, 1, idx].float().cpu().numpy(), rk) <= GRAD_REL_TOL
+    assert rel_fro(dv[0, 1, idx].float().cpu().numpy(), rv) <= GRAD_REL_TOL
