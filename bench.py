@@ -442,6 +442,87 @@ def run_softmax_rows(args):
         "gpu_launches": K}), flush=True)
 
 
+def _time_ms(fn, steps, warmup):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def run_splitkv(args):
+    """Split-KV forward on a small-batch shape whose plain grid leaves SMs idle: B=1, Hq=Hkv=8,
+    N=2048, d=128, causal (8 heads x 8 query-tile pairs = 64 work items for 152 SMs)."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    B, H, N, d = 1, 8, 2048, 128
+    q, k, v, _ = (t.cuda() if t is not None else None for t in make_qkv(B, H, H, N, d, seed=5, value_scale=0.5))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=q.device)
+    ws = torch.empty(fa.lib().fa_fwd_splitkv_workspace_bytes(B, H, H, N, d, 16), dtype=torch.uint8, device=q.device)
+    fl = fwd_flops(B, H, N, d, True)
+    t_plain = _time_ms(lambda: fa.forward(q, k, v, True, out=o, lse=lse), args.steps, args.warmup)
+    t_split = _time_ms(lambda: fa.forward_splitkv(q, k, v, True, 0, out=o, lse=lse, workspace=ws), args.steps,
+                       args.warmup)
+    fa.check()
+    print(json.dumps({
+        "metric": "split-KV forward TFLOP/s (bf16, B=1 H=8 N=2048 d=128 causal)",
+        "value": round(fl / (t_split * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_split, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": "fa_fwd_splitkv (automatic split count) vs fa_fwd"},
+        "plain_fwd": {"tflops": round(fl / (t_plain * 1e-3) / 1e12, 2), "ms": round(t_plain, 4)},
+        "speedup_vs_plain": round(t_plain / t_split, 3), "gpu_launches": 2 * args.steps}), flush=True)
+
+
+def run_window(args):
+    """Sliding-window attention, fwd + bwd, B=1, Hq=32, Hkv=8, N=32768, d=128, window 4096, against
+    full causal attention on the same inputs. FLOPs count visible (query, key) pairs only."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    B, Hq, Hkv, N, d, w = 1, 32, 8, 32768, 128, 4096
+    q, k, v, do = (t.cuda() for t in make_qkv(B, Hq, Hkv, N, d, seed=6, value_scale=0.5, with_do=True))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, N, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=q.device)
+    pairs = sum(min(i + 1, w) for i in range(N))
+    fl = 4 * d * pairs * B * Hq * (1 + BWD_FACTOR)
+    fl_causal = fwd_flops(B, Hq, N, d, True) * (1 + BWD_FACTOR)
+
+    def win():
+        fa.forward_window(q, k, v, w, out=o, lse=lse)
+        fa.backward_window(q, k, v, o, do, lse, w, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    def full():
+        fa.forward(q, k, v, True, out=o, lse=lse)
+        fa.backward(q, k, v, o, do, lse, True, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    t_win = _time_ms(win, args.steps, args.warmup)
+    t_full = _time_ms(full, args.steps, args.warmup)
+    fa.check()
+    print(json.dumps({
+        "metric": "sliding-window attention fwd+bwd TFLOP/s (bf16, N=32768, window 4096, d=128)",
+        "value": round(fl / (t_win * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_win, 4), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": "fa_fwd_window + fa_bwd_window, B=1 Hq=32 Hkv=8"},
+        "full_causal": {"tflops": round(fl_causal / (t_full * 1e-3) / 1e12, 2), "ms": round(t_full, 4)},
+        "time_ratio_full_over_window": round(t_full / t_win, 3), "visible_pair_ratio": round(N * (N + 1) / 2 / pairs, 3),
+        "gpu_launches": 8 * args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,13 +533,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
-    ap.add_argument("--workload", choices=["attention", "softmax_rows"], default="attention",
+    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window"], default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.workload == "softmax_rows":
         run_softmax_rows(args)
+    elif args.workload == "splitkv":
+        run_splitkv(args)
+    elif args.workload == "window":
+        run_window(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
