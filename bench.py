@@ -523,6 +523,34 @@ def run_window(args):
         "gpu_launches": 8 * args.steps}), flush=True)
 
 
+def run_naive(args):
+    """Standard attention with S and P in HBM (fa_naive_fwd) against the tiled kernel (fa_fwd), the
+    comparison of "LLM Architecture Refresh [3]", section 8 (8 heads, d=64, causal, N=512..4096)."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    rows = []
+    for N in (512, 1024, 2048, 4096):
+        q, k, v, _ = (t.cuda() if t is not None else None for t in make_qkv(1, 8, 8, N, 64, seed=7))
+        o = torch.empty_like(q)
+        lse = torch.empty(1, 8, N, device=q.device)
+        ws = torch.empty(int(fa.lib().fa_naive_workspace_bytes(1, 8, 8, N, 64)), dtype=torch.uint8, device=q.device)
+        t_naive = _time_ms(lambda: fa.forward_naive(q, k, v, True, out=o, lse=lse, workspace=ws), args.steps,
+                           args.warmup)
+        t_tiled = _time_ms(lambda: fa.forward(q, k, v, True, out=o, lse=lse), args.steps, args.warmup)
+        fa.check()
+        rows.append({"N": N, "naive_ms": round(t_naive, 4), "tiled_ms": round(t_tiled, 4),
+                     "speedup": round(t_naive / t_tiled, 2)})
+    print(json.dumps({
+        "metric": "tiled / naive attention speedup (bf16, B=1 H=8 d=64 causal)", "value": rows[-1]["speedup"],
+        "unit": "x at N=4096", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fa_naive_fwd (S fp32 and P bf16 through HBM, cuBLAS GEMMs) vs fa_fwd"},
+        "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,7 +561,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
-    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window"], default="attention",
+    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive"],
+                    default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -544,6 +573,8 @@ def main():
         run_splitkv(args)
     elif args.workload == "window":
         run_window(args)
+    elif args.workload == "naive":
+        run_naive(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

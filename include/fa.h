@@ -22,7 +22,8 @@
  * 16-byte aligned.
  *
  * Ownership. The caller allocates and owns every buffer, including the backward
- * workspace; the library never allocates device memory.
+ * workspace; the library never allocates device memory (except inside cuBLAS, which only the
+ * fa_naive_fwd baseline uses).
  *
  * Streams and errors. `stream` is a cudaStream_t (NULL = legacy default stream). Every call
  * is asynchronous on that stream. The return value reports argument errors (nothing is
@@ -186,6 +187,21 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    const float *lse, void *dq, void *dk, void *dv,
                    int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                    fa_stream_t stream);
+
+/*
+ * Baseline: standard attention with the N x N score matrix in HBM ("LLM Architecture
+ * Refresh [3]", section 1: S = QK^T written out, read back for P = softmax(S), written, read
+ * back for O = PV). S (fp32) and P (bf16) live in the workspace; the two products are cuBLAS
+ * batched GEMMs (fp32 accumulation), the masked softmax a kernel of this library. Same
+ * outputs as fa_fwd. Exists to measure what tiling saves; it needs O(B * Hq * N^2) bytes.
+ *   workspace: >= fa_naive_workspace_bytes() bytes, 16-byte aligned.
+ * cuBLAS is loaded at the first call (FA_ERR_UNSUPPORTED if it cannot be found) and keeps a
+ * handle, with its own device memory, per device.
+ */
+size_t fa_naive_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+int fa_naive_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 void *workspace, size_t workspace_bytes,
+                 int B, int Hq, int Hkv, int N, int d, int causal, float scale, fa_stream_t stream);
 
 /*
  * Row-wise softmax by the online normaliser ("LLM Architecture Refresh [3]", section 2, "Online

@@ -333,6 +333,24 @@ int fa_bwd_finalize(void* dq, void* workspace, size_t workspace_bytes, int B, in
                   workspace_bytes, B, Hq, Hkv, N, d, 0, scale, stream, fa::kBwdFinalize);
 }
 
+size_t fa_naive_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+  if (check_sizes(B, Hq, Hkv, N, d) != FA_OK) return 0;
+  return fa::naive_workspace_bytes(B, Hq, N);
+}
+
+int fa_naive_fwd(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                 size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                 fa_stream_t stream) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)}) FA_TRY(check_ptr(p));
+  if (workspace == nullptr || workspace_bytes < fa::naive_workspace_bytes(B, Hq, N)) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
+  FA_TRY(current_device(nullptr));
+  const int r = fa::launch_naive_fwd(q, k, v, o, lse, workspace, B, Hq, Hkv, N, d, causal ? 1 : 0,
+                                     resolve_scale(scale, d), reinterpret_cast<cudaStream_t>(stream));
+  return r == 0 ? FA_OK : (r == 1 ? FA_ERR_UNSUPPORTED : FA_ERR_LAUNCH);
+}
+
 int fa_softmax_rows(const float* x, float* p, float* lse, long long rows, int n, fa_stream_t stream) {
   if (rows < 1 || rows > 0x7fffffffLL || n < 1) return FA_ERR_INVALID;
   FA_TRY(check_ptr(x));

@@ -57,6 +57,12 @@ cudaError_t launch_bwd(const BwdLaunch& a, int stages);
 // Row-wise online softmax: x, p [rows][n] fp32, lse [rows] (nullable).
 cudaError_t launch_softmax_rows(const float* x, float* p, float* lse, long long rows, int n, cudaStream_t st);
 
+// Naive attention baseline (S and P in HBM): workspace bytes and launch (0 ok, 1 no cuBLAS,
+// 2 error).
+size_t naive_workspace_bytes(int B, int Hq, int N);
+int launch_naive_fwd(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int B,
+                     int Hq, int Hkv, int N, int d, int causal, float scale, cudaStream_t st);
+
 inline int round_up_tile(int n) { return (n + kTile - 1) / kTile * kTile; }
 
 }  // namespace fa

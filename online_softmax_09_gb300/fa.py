@@ -61,6 +61,10 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_splitkv.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
                                      ctypes.c_size_t, _vp]
         L.fa_fwd_splitkv.restype = _i
+        L.fa_naive_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.fa_naive_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_naive_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_naive_fwd.restype = _i
         L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]
         L.fa_softmax_rows.restype = _i
         L.fa_check.argtypes = [_vp]
@@ -139,6 +143,24 @@ def forward_splitkv(q, k, v, causal: bool = False, num_splits: int = 0, scale: f
                              workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
     if r != FA_OK:
         raise FAError(r, "fa_fwd_splitkv")
+    return o, l
+
+
+def forward_naive(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None,
+                  stream=None):
+    """Baseline standard attention with S and P in HBM (fa_naive_fwd)."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    o = out if out is not None else torch.empty_like(q)
+    l = lse if lse is not None else torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(int(lib().fa_naive_workspace_bytes(B, Hq, Hkv, N, d)), dtype=torch.uint8,
+                                device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_naive_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), B, Hq, Hkv, N, d, int(bool(causal)), sc,
+                           _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_naive_fwd")
     return o, l
 
 
