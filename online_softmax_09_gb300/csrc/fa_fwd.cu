@@ -22,8 +22,15 @@
 //
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // The running max is kept in base-2 units (scores scaled by scale*log2 e) so P uses the
-// hardware exp2. The max is the true running max: l and O are rescaled whenever a tile raises
-// it, so the largest weight of each row is exactly 1 and loses nothing to bf16 rounding.
+// hardware exp2. P is taken against a reference max m_ref that follows the true running max
+// lazily: a warp rescales l and O (and moves m_ref of its rows to their true max) only when one
+// of its rows' max has risen more than kRescaleLog2 above m_ref; otherwise weights up to
+// 2^kRescaleLog2 are used as they are. Any reference gives the same softmax (the correction
+// factors cancel between O and l), so this only skips the O pass on most tiles. A weight above 1
+// is generally not a bf16 number, and the P.V MMA consumes it rounded while l holds it exact: for
+// a row dominated by one key that mismatch would show in O at bf16's relative precision. So each
+// tile's largest weight is recomputed exactly as pass 2 computes it, its bf16 rounding error is
+// accumulated in e (rescaled like l), and O is divided by l + e; LSE keeps the fp32 l.
 // S is read from TMEM twice (once for the row max, once for P) to keep registers low.
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -144,6 +151,9 @@ struct FwdSmem {
 };
 
 constexpr int kFwdThreads = 320;
+// A warp rescales when a row's max exceeds its reference by more than this (base 2): weights
+// stay below 2^8, far inside fp32 and bf16 range.
+constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kNegInf = 0xff800000u;
 
@@ -382,9 +392,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         continue;
       }
       const int jbase = itm.j0 + a_t;  // absolute index of the first key tile
-      float m_run = -INFINITY;
+      float m_run = -INFINITY;  // reference max (base 2) of P, l and O
+      float m_hi = -INFINITY;   // true running max (base 2)
       float l_run = 0.f;
-      uint32_t n_rescaled = 0;
+      float e_run = 0.f;        // bf16 rounding error of the tile maxima's weights (see above)
+      uint32_t n_raised = 0;
       for (int j = 0; j < n_kv; ++j) {
         if (!mbar_wait_warp(bar(L::bSFull + t), (sc + j) & 1, ctl)) {
           ok = false;
@@ -412,12 +424,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           mx = max64(a, b2, mx);
         }
-        // Running max in base-2 units; correction exp(m_old - m_new) (0 on the first tile).
-        const float m_new = fmaxf(m_run, mx * sl2);
+        // Reference max in base-2 units, moved to the true max only when some row of the warp
+        // has outgrown it by more than kRescaleLog2 (always on the first tile, where
+        // m_run = -inf); correction exp(m_old - m_new) (0 on the first tile).
+        const float mt = mx * sl2;
+        if (j > 0 && mt > m_hi && row < p.N) ++n_raised;  // the true running max rose
+        m_hi = fmaxf(m_hi, mt);
+        const bool resc = __any_sync(0xffffffffu, m_hi > m_run + kRescaleLog2);
+        const float m_new = resc ? m_hi : m_run;
         const float corr = (m_new > m_run) ? ex2(m_run - m_new) : 1.f;
-        if (j > 0 && m_new > m_run && row < p.N) ++n_rescaled;
         m_run = m_new;
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        {
+          // This tile's largest weight, bit-identical to its value in pass 2 (same correctly
+          // rounded fma and exp2), and the error its bf16 rounding makes in the P.V MMA.
+          const float pmx = ex2(fmaf(mx, sl2, -m_use));
+          e_run = e_run * corr + (__uint_as_float(pack_bf16(pmx, 0.f) << 16) - pmx);
+        }
         if (j > 0) {
           // O += P_{j-1} V has completed before S_j did; this wait at every tile keeps the
           // warp's view of the barrier phase exact and returns at once.
@@ -425,7 +448,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ok = false;
             break;
           }
-          if (__any_sync(0xffffffffu, corr != 1.f)) {
+          if (resc) {
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -474,7 +497,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!(ok = mbar_wait_warp(bar(L::bOFull + t), (sc + n_kv - 1) & 1, ctl))) break;
       sc += n_kv;
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = 1.f / (l_run + e_run);
       if (kSplit) {
         // Split mode: the partial output acc / l (fp32) and its LSE, merged later.
         if (row < p.N) p.lse_part[part_row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
@@ -522,7 +545,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         p.lse[(size_t)itm.bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
       }
       if (!kSplit && p.counters != nullptr) {
-        unsigned int r = n_rescaled;
+        unsigned int r = n_raised;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
         if (lane == 0 && r) atomicAdd(&p.counters[2], (unsigned long long)r);
