@@ -372,7 +372,7 @@ int fa_check(fa_stream_t stream) {
   if (h != 0) {
     const uint32_t zero = 0;
     if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_LAUNCH;
-    return FA_ERR_TIMEOUT;
+    return h == 1 ? FA_ERR_TIMEOUT : FA_ERR_LAUNCH;  // 2: a kernel found its shared memory misaligned
   }
   return FA_OK;
 }

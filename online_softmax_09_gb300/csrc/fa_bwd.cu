@@ -23,9 +23,14 @@
 //      the dK and dQ MMAs run, so the tensor core does not wait for the softmax warps.
 //   3. dQ conversion: dq = bf16(scale * accumulator).
 //
-// Warp roles of the main kernel: 0-3 softmax/dS and the final dK/dV epilogue, 4 TMA producer,
-// 5 MMA issuer and TMEM owner, 6-9 dQ drain.
+// Warp roles of the main kernel: 0-3 and 10-13 softmax/dS (thread = key row; warps 0-3 take
+// query columns [0, 64) of every row, warps 10-13 columns [64, 128), so each row's elementwise
+// work is split between two warps of the same TMEM lane quarter), then the final dV (0-3) and
+// dK (10-13) epilogue; 4 TMA producer, 5 MMA issuer and TMEM owner, 6-9 dQ drain.
 // TMEM columns: S^T/P^T [0,128), dP^T/dS^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+// P^T and dS^T are packed bf16 (two queries per column): queries [0, 64) in columns [0, 32) of
+// their region, queries [64, 128) in [64, 96), i.e. each half over score columns its own warps
+// have already read.
 // For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
 // once the dV and dP MMAs (the readers of dO) have completed; for D = 64 it has its own buffer.
 #include "fa_internal.h"
@@ -130,9 +135,9 @@ struct BwdSmem {
   static constexpr int kStD = 2 * kTileBytes + 512;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kDS = kStage0 + 2 * kStageBytes;
-  // dQ staging for the bulk reductions: 4 drain warps x 32 rows x 128 bytes.
+  // dQ staging for the bulk reductions: 4 drain warps x 2 buffers x 32 rows x 128 bytes.
   static constexpr int kDQ = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
-  static constexpr int kBar = kDQ + 4 * 32 * 128;
+  static constexpr int kBar = kDQ + 4 * 2 * 32 * 128;
   enum {
     bKV = 0,
     bQFull = 1,       // 2
@@ -152,12 +157,16 @@ struct BwdSmem {
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
-  static constexpr int kAlloc = kBytes + 1024;
+  // No alignment slack: the kernel uses no static shared memory, so the dynamic window starts
+  // on a 1024-byte boundary; the kernel checks this and stops (status 2) if it ever does not.
+  static constexpr int kAlloc = kBytes;
   static_assert(kStageBytes % 1024 == 0 && kStage0 % 1024 == 0 && kDS % 1024 == 0 && kDQ % 1024 == 0,
                 "1024-byte alignment");
 };
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
+// TMEM column of the packed bf16 operand (P^T or dS^T) for the 16 queries of MMA step kk.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
 
 template <int D, bool kWin>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -167,7 +176,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  if (raw & 1023u) {  // uniform over the CTA, before any barrier or tensor memory is touched
+    if (threadIdx.x == 0) atomicCAS(p.status, kStatusOk, kStatusSmemAlign);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase + L::kK;
   const uint32_t sV = sbase + L::kV;
@@ -210,9 +223,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bDPFull), 1);
-    mbar_init(bar(L::bPReady), 128);
-    mbar_init(bar(L::bDSReady), 128);
-    mbar_init(bar(L::bSmemDS), 128);
+    mbar_init(bar(L::bPReady), 256);
+    mbar_init(bar(L::bDSReady), 256);
+    mbar_init(bar(L::bSmemDS), 256);
     mbar_init(bar(L::bDQFull), 1);
     mbar_init(bar(L::bDQFree), 128);
     mbar_init(bar(L::bFinal), 1);
@@ -314,7 +327,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdV, tS + kk * 8, sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+          mma_ts(tdV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
         // dP^T = V_n dO_i^T, once the previous dQ has been drained out of these columns.
         if (it > 0 && !(ok = mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl))) break;
         tc_fence_after();
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdK, tdP + kk * 8, sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+          mma_ts(tdK, tdP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
         // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns
         if (!(ok = mbar_wait(bar(L::bSmemDS), it & 1, ctl))) break;
         tc_fence_after();
@@ -353,15 +366,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         drain_wait(bar(L::bDrain), 0);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 10) {
     // ------------------------------------------------------------------ softmax / dS warps
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int kr = threadIdx.x;  // key row within the tile
+    const int grp = warp >= 10;  // query columns [64 grp, 64 grp + 64) of each key row
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int kr = (warp & 3) * 32 + lane;  // key row within the tile
     const int key = n * kTile + kr;
     const bool key_ok = key < p.N;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    uint32_t pk[4][16];  // P_it^T as packed bf16, kept from the P phase to the dS phase
+    uint32_t pk[2][16];  // this warp's half of P_it^T as packed bf16, kept for the dS phase
     // P phase of query tile `it`: P^T = 2^(S^T scale log2e - LSE2), bf16 into TMEM and pk.
     auto p_phase = [&](int it) -> bool {
       const int s = it & 1;
@@ -375,7 +389,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!mbar_wait_warp(bar(L::bSFull), it & 1, ctl)) return false;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * grp + cc;  // 32-query chunk
         uint32_t sr[32];
         tmem_ld32(tS + lane_off + c * 32, sr);
         tmem_ld_wait(sr);
@@ -390,11 +405,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pv[t] = ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
             if (!key_ok || (diag && q < kr) || (wmask && (i - n) * kTile + q - kr >= p.window)) pv[t] = 0.f;
           }
-          pk[c][j / 2] = pack_bf16(pv[0], pv[1]);
-          pk[c][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
+          pk[cc][j / 2] = pack_bf16(pv[0], pv[1]);
+          pk[cc][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
         }
-        // P^T (bf16) overwrites S^T columns [16c, 16c+16), all of which were read already.
-        tmem_st16(tS + lane_off + c * 16, pk[c]);
+        // P^T (bf16) of chunk c into columns [64 grp + 16 cc, +16): score columns this warp
+        // has already read.
+        tmem_st16(tS + lane_off + 64 * grp + 16 * cc, pk[cc]);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -412,7 +428,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // implies every earlier MMA is, so the dO slot (or the dS buffer) is free to overwrite.
       const uint32_t row_base = sDS(s) + (uint32_t)kr * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * grp + cc;
         uint32_t dr[32];
         tmem_ld32(tdP + lane_off + c * 32, dr);
         tmem_ld_wait(dr);
@@ -420,20 +437,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           const float4 d4 = *reinterpret_cast<const float4*>(sd + c * 32 + j);
-          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][j / 2]));
-          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c][j / 2 + 1]));
+          const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[cc][j / 2]));
+          const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[cc][j / 2 + 1]));
           ds[j / 2] = pack_bf16(p01.x * (__uint_as_float(dr[j + 0]) - d4.x),
                                 p01.y * (__uint_as_float(dr[j + 1]) - d4.y));
           ds[j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
                                     p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
         }
-        tmem_st16(tdP + lane_off + c * 16, ds);
+        tmem_st16(tdP + lane_off + 64 * grp + 16 * cc, ds);
         // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
         // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
-          const int g = (c & 1) * 4 + g4;
-          st_shared_v4(row_base + (c >> 1) * 16384 + ((g ^ (kr & 7)) << 4), ds[4 * g4], ds[4 * g4 + 1],
+          const int g = cc * 4 + g4;
+          st_shared_v4(row_base + grp * 16384 + ((g ^ (kr & 7)) << 4), ds[4 * g4], ds[4 * g4 + 1],
                        ds[4 * g4 + 2], ds[4 * g4 + 3]);
         }
       }
@@ -444,70 +461,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar(L::bSmemDS));
       if (it + 1 < n_iter && !(ok = p_phase(it + 1))) break;
     }
-    // ---------------------------------------------------------------- dK / dV epilogue
+    // ---------------------------------------------------------------- dV (0-3) / dK (10-13) epilogue
     if (ok) ok = mbar_wait_warp(bar(L::bFinal), 0, ctl);
     if (ok) {
       tc_fence_after();
       const size_t row_off = ((size_t)(b * p.Hkv + hkv) * p.N + key) * D;
+      const uint32_t src = grp ? tdK : tdV;
+      const float mul = grp ? p.scale : 1.f;
+      __nv_bfloat16* dst_base = grp ? p.dk : p.dv;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t src = which ? tdK : tdV;
-        const float mul = which ? p.scale : 1.f;
-        __nv_bfloat16* dst_base = which ? p.dk : p.dv;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(src + lane_off + c * 32, a);
+        tmem_ld_wait(a);
+        uint4 w[4];
+        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(src + lane_off + c * 32, a);
-          tmem_ld_wait(a);
-          uint4 w[4];
-          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+        for (int j = 0; j < 16; ++j)
+          wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = w[j];
-          }
+          for (int j = 0; j < 4; ++j) dst[j] = w[j];
         }
       }
     }
   } else {
     // ------------------------------------------------------------------ dQ drain warps 6-9
-    // Each warp owns 32 query rows (its TMEM lane quarter). dQ_i leaves TMEM at once (so the
-    // next dP MMA can reuse the columns); then, 32 columns at a time, the warp stages its
-    // 32 x 32 fp32 block in shared memory (128-byte swizzled: 16-byte granule g of row r at
-    // g ^ (r mod 8)) and one lane adds it into the workspace accumulator with a bulk tensor
-    // reduction. Warps never wait for one another.
+    // Each warp owns 32 query rows (its TMEM lane quarter). 32 columns at a time, the warp
+    // stages its 32 x 32 fp32 block of dQ_i in shared memory (128-byte swizzled: 16-byte granule
+    // g of row r at g ^ (r mod 8)) and one lane adds it into the workspace accumulator with a
+    // bulk tensor reduction. Warps never wait for one another.
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t stage_buf = sbase + L::kDQ + (uint32_t)(warp & 3) * 4096;
-    const uint32_t my_row = stage_buf + (uint32_t)lane * 128;
+    const uint32_t stage_buf = sbase + L::kDQ + (uint32_t)(warp & 3) * 8192;
     for (int it = 0; it < n_iter; ++it) {
       int hq, i;
       item(it, hq, i);
       if (!mbar_wait_warp(bar(L::bDQFull), it & 1, ctl)) break;
       tc_fence_after();
-      uint32_t a[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tdP + lane_off + c * 32, a[c]);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(a[c]);
-      tc_fence_before();
-      mbar_arrive(bar(L::bDQFree));
       const int row0 = (b * p.Hq + hq) * p.Npad + i * kTile + (warp & 3) * 32;
+      // Two halves of 64 columns (the register budget of 14 warps), each chunk staged through
+      // buffer (chunk mod 2): a buffer is rewritten only after the reduction issued from it
+      // two chunks earlier has read it, so the first half never waits for a reduction and the
+      // columns are released right after the second half is loaded.
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (lane == 0) bulk_wait_read_all();  // the previous block has left the staging buffer
-        __syncwarp();
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t a[2][32];
+        tmem_ld32(tdP + lane_off + (2 * h) * 32, a[0]);
+        tmem_ld32(tdP + lane_off + (2 * h + 1) * 32, a[1]);
+        tmem_ld_wait(a[0]);
+        tmem_ld_wait(a[1]);
+        if (h == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(L::bDQFree));
+        }
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-          st_shared_v4(my_row + ((g ^ (lane & 7)) << 4), a[c][4 * g], a[c][4 * g + 1], a[c][4 * g + 2],
-                       a[c][4 * g + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&tm_dq, stage_buf, c * 32, row0);
-          bulk_commit_group();
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * h + cc;
+          const uint32_t buf = stage_buf + (uint32_t)cc * 4096;
+          if (lane == 0) bulk_wait_read_but1();  // the reduction from this buffer has read it
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            st_shared_v4(buf + (uint32_t)lane * 128 + ((g ^ (lane & 7)) << 4), a[cc][4 * g], a[cc][4 * g + 1],
+                         a[cc][4 * g + 2], a[cc][4 * g + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_dq, buf, c * 32, row0);
+            bulk_commit_group();
+          }
         }
       }
     }

@@ -14,7 +14,7 @@ namespace fa {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Status codes written to the device status word (first failure wins).
-enum : uint32_t { kStatusOk = 0, kStatusTimeout = 1 };
+enum : uint32_t { kStatusOk = 0, kStatusTimeout = 1, kStatusSmemAlign = 2 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -322,6 +322,10 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Waits until every committed bulk group has completed.
+// All but the most recently committed bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_but1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 }  // namespace fa
