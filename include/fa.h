@@ -189,6 +189,32 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
                    fa_stream_t stream);
 
 /*
+ * Forward and backward pass of one attention layer on HOST buffers: the computations of
+ * fa_fwd then fa_bwd ("LLM Architecture Refresh [3]", sections 4 and 8) with the
+ * host<->device copies done by the library and overlapped with the kernels. The pages have no
+ * counterpart for the data movement.
+ *   q, k, v, dout: host inputs, same layouts and types as fa_fwd / fa_bwd.
+ *   o (bf16), lse (fp32), dq, dk, dv (bf16): host outputs, same layouts as there.
+ *   workspace: device memory of at least fa_fwd_bwd_host_workspace_bytes(...) bytes, 256-byte
+ *     aligned; it holds device copies of all nine tensors and a backward workspace.
+ * The work runs batch element by batch element: while the kernels of element b run on
+ * `stream`, the inputs of later elements are copied in and the outputs of earlier ones out on
+ * two streams the library creates once per device. Host buffers must be page-locked (pinned)
+ * for the copies to overlap; pageable buffers give correct results without the overlap. The
+ * call is asynchronous like the others: the outputs are complete once `stream` has passed this
+ * call (e.g. after fa_check(stream)), and the call starts after everything enqueued on `stream`
+ * before it. Calls on one device are serialised by the library on the host. Errors as for
+ * fa_fwd and fa_bwd, plus FA_ERR_WORKSPACE (workspace missing or too small) and FA_ERR_ALIGN
+ * (workspace not 256-byte aligned); after an error some copies or kernels may already have
+ * been enqueued and the outputs are undefined.
+ */
+size_t fa_fwd_bwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+int fa_fwd_bwd_host(const void *q, const void *k, const void *v, const void *dout,
+                    void *o, float *lse, void *dq, void *dk, void *dv,
+                    int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                    void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Baseline: standard attention with the N x N score matrix in HBM ("LLM Architecture
  * Refresh [3]", section 1: S = QK^T written out, read back for P = softmax(S), written, read
  * back for O = PV). S (fp32) and P (bf16) live in the workspace; the two products are cuBLAS

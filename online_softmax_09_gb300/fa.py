@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
         L.fa_naive_workspace_bytes.restype = ctypes.c_size_t
         L.fa_naive_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_naive_fwd.restype = _i
+        L.fa_fwd_bwd_host_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+        L.fa_fwd_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_fwd_bwd_host.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _i, _i, _f, _vp, ctypes.c_size_t, _vp]
+        L.fa_fwd_bwd_host.restype = _i
         L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]
         L.fa_softmax_rows.restype = _i
         L.fa_check.argtypes = [_vp]
@@ -233,6 +237,53 @@ def backward_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, causal: bool = F
     if between is not None:
         between(3)
     return dq, dk, dv
+
+
+def fwd_bwd_host_workspace_bytes(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    """Device workspace bytes for fa_fwd_bwd_host."""
+    n = lib().fa_fwd_bwd_host_workspace_bytes(B, Hq, Hkv, N, d)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return n
+
+
+def fwd_bwd_host(q, k, v, do, causal: bool = False, scale: float | None = None, out=None, workspace=None,
+                 device=None, stream=None):
+    """Forward and backward on host (CPU, ideally pinned) bf16 tensors (fa_fwd_bwd_host).
+
+    Returns host tensors ``(o, lse, dq, dk, dv)``; ``out`` may supply them (o, dq, dk, dv bf16
+    and lse fp32, contiguous CPU tensors). ``workspace`` is a CUDA uint8 tensor of at least
+    fwd_bwd_host_workspace_bytes(...) bytes (allocated when None). Asynchronous: the outputs
+    are ready after the stream is synchronised (e.g. check())."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D bfloat16 CPU tensor [B, H, N, d]")
+    B, Hq, N, d = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or do.shape != q.shape:
+        raise ValueError("k, v must be [B, Hkv, N, d] and do [B, Hq, N, d] with the same B, N, d as q")
+    Hkv = k.shape[1]
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        pin = q.is_pinned()
+        out = (torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin),
+               torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin),
+               torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin),
+               torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=pin),
+               torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=pin))
+    o, lse, dq, dk, dv = out
+    for t, shape, dt in ((o, q.shape, torch.bfloat16), (lse, (B, Hq, N), torch.float32), (dq, q.shape, torch.bfloat16),
+                         (dk, k.shape, torch.bfloat16), (dv, k.shape, torch.bfloat16)):
+        if t.is_cuda or tuple(t.shape) != tuple(shape) or t.dtype != dt or not t.is_contiguous():
+            raise ValueError("out must be contiguous CPU tensors (o, lse, dq, dk, dv) of the input shapes")
+    nbytes = fwd_bwd_host_workspace_bytes(B, Hq, Hkv, N, d)
+    ws = workspace if workspace is not None else torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_fwd_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), sc,
+                              ws.data_ptr(), ws.numel() * ws.element_size(), _stream_handle(stream, dev))
+    if r != FA_OK:
+        raise FAError(r, "fa_fwd_bwd_host")
+    return o, lse, dq, dk, dv
 
 
 def softmax_rows(x, out=None, lse=None, with_lse: bool = True, stream=None):

@@ -72,3 +72,20 @@ def test_workspace_size_is_linear_in_n(L):
     assert L.fa_bwd(*args, 0x1000, 0, 1, 1, 1, 128, 128, 0, 0.0, None) == -6  # workspace too small
     assert L.fa_bwd(*args, None, 1 << 30, 1, 1, 1, 128, 128, 0, 0.0, None) == -6
     assert L.fa_bwd(*args, 0x1001, 1 << 30, 1, 1, 1, 128, 128, 0, 0.0, None) == -3
+
+
+def test_host_step_workspace_and_argument_errors(L):
+    a = lambda x: (x + 255) // 256 * 256
+    B, Hq, Hkv, N, d = 2, 8, 2, 1000, 128
+    q, kv, lse = Hq * N * d * 2, Hkv * N * d * 2, Hq * N * 4
+    want = 4 * a(B * q) + 4 * a(B * kv) + a(B * lse) + a(L.fa_bwd_workspace_bytes(1, Hq, Hkv, N, d))
+    assert L.fa_fwd_bwd_host_workspace_bytes(B, Hq, Hkv, N, d) == want
+    assert L.fa_fwd_bwd_host_workspace_bytes(B, 3, 2, N, d) == 0  # Hq % Hkv != 0
+    assert L.fa_fwd_bwd_host_workspace_bytes(0, Hq, Hkv, N, d) == 0
+    ptrs = [0x1000] * 9
+    ws = L.fa_fwd_bwd_host_workspace_bytes(1, 1, 1, 128, 128)
+    assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 128, 0, 0.0, 0x1000, ws - 1, None) == -6  # too small
+    assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 128, 0, 0.0, None, ws, None) == -6
+    assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 128, 0, 0.0, 0x1080, ws, None) == -3  # not 256-aligned
+    assert L.fa_fwd_bwd_host(None, *ptrs[1:], 1, 1, 1, 128, 128, 0, 0.0, 0x1000, ws, None) == -1
+    assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 96, 0, 0.0, 0x1000, ws, None) == -1  # d = 96: no layout
