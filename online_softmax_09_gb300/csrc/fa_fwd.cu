@@ -287,9 +287,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t gk = 0, gv = 0;  // K and V tiles consumed so far
       uint32_t qn[2] = {0, 0};  // items in which query tile t was active
       uint32_t pc[2] = {0, 0};  // P.V MMAs issued for tile t
-      auto issue_s = [&](int t, uint32_t g) -> bool {  // S_t = Q_t K^T with K tile number g
+      // S_t = Q_t K^T with K tile number g; `ready`: K tile g's full barrier was already waited
+      // on for the other query tile.
+      auto issue_s = [&](int t, uint32_t g, bool ready) -> bool {
         const uint32_t sk = g % NK;
-        if (!mbar_wait(bar(L::bKFull + sk), (g / NK) & 1, ctl)) return false;
+        if (!ready && !mbar_wait(bar(L::bKFull + sk), (g / NK) & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t q_base = sQ + t * L::kTileBytes;
         const uint32_t k_base = sK + sk * L::kTileBytes;
@@ -303,10 +305,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(bar(L::bSFull + t));
         return true;
       };
-      auto issue_pv = [&](int t, uint32_t g, bool first) -> bool {  // O_t += P_t V, V tile number g
+      // O_t += P_t V with V tile number g. O_t's completion is signalled only after an item's last
+      // P.V (for the epilogue): each earlier one is followed by S_t's next score MMA, whose
+      // completion (which the softmax warps wait for) implies it.
+      auto issue_pv = [&](int t, uint32_t g, bool first, bool last, bool ready) -> bool {
         const uint32_t sv = g % NV;
         if (!mbar_wait(bar(L::bPFull + t), pc[t] & 1, ctl)) return false;
-        if (!mbar_wait(bar(L::bVFull + sv), (g / NV) & 1, ctl)) return false;
+        if (!ready && !mbar_wait(bar(L::bVFull + sv), (g / NV) & 1, ctl)) return false;
         // The first P.V of an item overwrites O_t: the previous item's epilogue must be done.
         if (first && qn[t] > 1 && !mbar_wait(bar(L::bOFree + t), (qn[t] - 2) & 1, ctl)) return false;
         tc_fence_after();
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024),
                  idO, (!first || kk > 0));
         }
-        mma_commit(bar(L::bOFull + t));
+        if (last) mma_commit(bar(L::bOFull + t));
         ++pc[t];
         return true;
       };
@@ -327,6 +332,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (k < 0) continue;
         const FwdItem it = fwd_item<kWin, kSplit>(k, p);
         if (it.n_max == 0) continue;
+        bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok) break;
@@ -335,18 +341,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++qn[t];
           tc_fence_after();
           if (it.a[t] == 0) {  // score MMA of the item's first key tile
-            if (!(ok = issue_s(t, gk))) break;
+            if (!(ok = issue_s(t, gk, k_ready))) break;
+            k_ready = true;
             if (it.b[t] == 1) mma_commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
           }
         }
         if (!ok) break;
         mma_commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
         for (int j = 0; ok && j < it.n_max; ++j) {
+          bool v_ready = false, k_next_ready = false;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (it.a[t] <= j && j < it.b[t] && !(ok = issue_pv(t, gv + j, j == it.a[t]))) break;
+            if (it.a[t] <= j && j < it.b[t]) {
+              if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
+              v_ready = true;
+            }
             if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
-              if (!(ok = issue_s(t, gk + j + 1))) break;
+              if (!(ok = issue_s(t, gk + j + 1, k_next_ready))) break;
+              k_next_ready = true;
               if (j + 2 == it.b[t]) mma_commit(bar(L::bQEmpty + t));
             }
           }
@@ -370,6 +382,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
     const float sl2 = p.scale_log2;
     uint32_t sc = 0;  // score tiles of this query tile processed so far (all items)
+    uint32_t on = 0;  // items of this query tile whose output was completed
     bool ok = true;
     for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
       const int k = fwd_item_index(r, p.num_items);
@@ -442,14 +455,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           e_run = e_run * corr + (__uint_as_float(pack_bf16(pmx, 0.f) << 16) - pmx);
         }
         if (j > 0) {
-          // O += P_{j-1} V has completed before S_j did; this wait at every tile keeps the
-          // warp's view of the barrier phase exact and returns at once.
-          if (!mbar_wait_warp(bar(L::bOFull + t), (sc + j - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
+          // O += P_{j-1} V was issued before S_j and has completed with it.
           if (resc) {
-            tc_fence_after();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -494,7 +501,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      if (!(ok = mbar_wait_warp(bar(L::bOFull + t), (sc + n_kv - 1) & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bOFull + t), on & 1, ctl))) break;  // the item's last P.V
+      ++on;
       sc += n_kv;
       tc_fence_after();
       const float inv_l = 1.f / (l_run + e_run);
