@@ -15,22 +15,23 @@
 //      group and their query tiles (causal: from the diagonal tile on). Per query tile i:
 //        softmax warps (thread = key row): P_i^T = 2^(S_i^T scale log2e - LSE2), bf16 -> TMEM
 //        MMA  dV += P_i^T dO_i ;  dP_i^T = V_n dO_i^T ;  S_{i+1}^T = K_n Q_{i+1}^T
-//        softmax warps: dS_i^T = P_i^T (dP_i^T - delta), bf16 -> TMEM and -> shared memory
-//        MMA  dK += dS_i^T Q_i ;  dQ_i = dS_i K_n  (into the dP^T columns, now free)
+//        softmax warps: dS_i^T = P_i^T (dP_i^T - delta), bf16 -> shared memory
+//        MMA  dQ_i = dS_i K_n  (into the dP^T columns, now free) ;  dK += dS_i^T Q_i
 //        drain warps (thread = query row): dQ_i TMEM -> shared memory -> bulk tensor
 //        reduction (add) into the fp32 workspace accumulator.
 //      The next tile's S^T is computed while the softmax warps work on dS_i, and its P while
-//      the dK and dQ MMAs run, so the tensor core does not wait for the softmax warps.
+//      the dQ and dK MMAs run, so the tensor core does not wait for the softmax warps. The one
+//      shared-memory copy of dS serves both of its MMAs (MN-major A of dQ, K-major A of dK),
+//      and dQ goes first so that its drain overlaps the dK MMA.
 //   3. dQ conversion: dq = bf16(scale * accumulator).
 //
 // Warp roles of the main kernel: 0-3 and 10-13 softmax/dS (thread = key row; warps 0-3 take
 // query columns [0, 64) of every row, warps 10-13 columns [64, 128), so each row's elementwise
 // work is split between two warps of the same TMEM lane quarter), then the final dV (0-3) and
 // dK (10-13) epilogue; 4 TMA producer, 5 MMA issuer and TMEM owner, 6-9 dQ drain.
-// TMEM columns: S^T/P^T [0,128), dP^T/dS^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
-// P^T and dS^T are packed bf16 (two queries per column): queries [0, 64) in columns [0, 32) of
-// their region, queries [64, 128) in [64, 96), i.e. each half over score columns its own warps
-// have already read.
+// TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
+// P^T is packed bf16 (two queries per column): queries [0, 64) in columns [0, 32), queries
+// [64, 128) in [64, 96), i.e. each half over score columns its own warps have already read.
 // For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
 // once the dV and dP MMAs (the readers of dO) have completed; for D = 64 it has its own buffer.
 #include "fa_internal.h"
@@ -146,7 +147,6 @@ struct BwdSmem {
     bSFull = 7,
     bDPFull,
     bPReady,
-    bDSReady,
     bSmemDS,
     bDQFull,
     bDQFree,
@@ -165,7 +165,7 @@ struct BwdSmem {
 };
 
 constexpr int kBwdThreads = 448;
-// TMEM column of the packed bf16 operand (P^T or dS^T) for the 16 queries of MMA step kk.
+// TMEM column of the packed bf16 P^T operand for the 16 queries of MMA step kk.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
 
 template <int D, bool kWin>
@@ -224,7 +224,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bDPFull), 1);
     mbar_init(bar(L::bPReady), 256);
-    mbar_init(bar(L::bDSReady), 256);
     mbar_init(bar(L::bSmemDS), 256);
     mbar_init(bar(L::bDQFull), 1);
     mbar_init(bar(L::bDQFree), 128);
@@ -249,7 +248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem;         // S^T, then P^T (bf16)
-  const uint32_t tdP = tmem + 128;  // dP^T, then dS^T (bf16), then dQ
+  const uint32_t tdP = tmem + 128;  // dP^T, then dQ
   const uint32_t tdV = tmem + 256;
   const uint32_t tdK = tmem + 256 + D;
 
@@ -296,8 +295,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
     // Per query tile i: dV += P_i^T dO_i, dP_i^T = V dO_i^T, S_{i+1}^T = K Q_{i+1}^T,
-    // dK += dS_i^T Q_i, dQ_i = dS_i K. The softmax warps compute dS_i while S_{i+1}^T runs and
-    // P_{i+1} while dK and dQ run; the dQ drain overlaps the next dV.
+    // dQ_i = dS_i K, dK += dS_i^T Q_i. The softmax warps compute dS_i while S_{i+1}^T runs and
+    // P_{i+1} while dQ and dK run; the dQ drain overlaps dK and the next dV.
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
@@ -343,13 +342,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           issue_s(it + 1);
         }
-        // dK += dS^T Q_i
-        if (!(ok = mbar_wait(bar(L::bDSReady), it & 1, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdK, tdP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
-        // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns
+        // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns, first,
+        // so the drain starts as early as possible; then dK += dS^T Q_i with the same
+        // shared-memory dS as the K-major A operand.
         if (!(ok = mbar_wait(bar(L::bSmemDS), it & 1, ctl))) break;
         tc_fence_after();
         const uint32_t sds = sDS(s);
@@ -358,6 +353,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(tdP, sdesc_sw128(sds + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ,
                  kk > 0);
         mma_commit(bar(L::bDQFull));
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tdK, sdesc_sw128(sds + off, 16, 1024), sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS,
+                 (it > 0 || kk > 0));
+        }
         mma_commit(bar(L::bStageEmpty + s));
       }
       if (ok) mma_commit(bar(L::bFinal));
@@ -444,7 +445,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds[j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
                                     p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
         }
-        tmem_st16(tdP + lane_off + 64 * grp + 16 * cc, ds);
         // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
         // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
 #pragma unroll
@@ -454,9 +454,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        ds[4 * g4 + 2], ds[4 * g4 + 3]);
         }
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(L::bDSReady));
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bSmemDS));
       if (it + 1 < n_iter && !(ok = p_phase(it + 1))) break;

@@ -4,10 +4,11 @@
 // The computation is fa_fwd followed by fa_bwd ("LLM Architecture Refresh [3]: Flash Attention
 // Is Exact", sections 4 and 8), run once per batch element on that element's slices of the
 // [B][H][N][d] tensors (contiguous in this layout). Three streams carry a software pipeline:
-//   input stream   copies q, k, v, dO of element b+1 to the device,
+//   input stream   copies q, k, v, then dO of element b+1 to the device,
 //   caller stream  runs the forward and backward kernels of element b,
-//   output stream  copies o, lse, dq, dk, dv of element b-1 back to the host,
-// ordered by one event per element and direction. GB300's copy engines move host data at about
+//   output stream  copies o, lse of element b once its forward is done, then dq, dk, dv once
+//                  its backward is,
+// ordered by events (each element's forward waits only for q, k, v; its backward for dO). GB300's copy engines move host data at about
 // 200 GB/s per direction and both directions at once, so for large steps the copies hide behind
 // the kernels except for the first element's inputs and the last element's outputs.
 // The input and output streams and the events are created once per device and reused; device
@@ -25,7 +26,7 @@ namespace {
 struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
-  std::vector<cudaEvent_t> ev;  // [0] start, [1] done, then 2 per batch element
+  std::vector<cudaEvent_t> ev;  // [0] start, [1] done, then 4 per batch element
 };
 HostPipe g_pipe[64];
 std::mutex g_pipe_mutex;
@@ -57,7 +58,7 @@ cudaEvent_t* pipe_events(int dev, int B) {
     if (cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
     P.ready = true;
   }
-  while ((int)P.ev.size() < 2 + 2 * B) {
+  while ((int)P.ev.size() < 2 + 4 * B) {
     cudaEvent_t e;
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     P.ev.push_back(e);
@@ -109,8 +110,10 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
   if (ev == nullptr) return FA_ERR_LAUNCH;
   HostPipe& P = g_pipe[dev];
   cudaEvent_t ev_start = ev[0], ev_done = ev[1];
-  cudaEvent_t* ev_in = ev + 2;
-  cudaEvent_t* ev_comp = ev + 2 + B;
+  cudaEvent_t* ev_qkv = ev + 2;          // q, k, v of element b on the device
+  cudaEvent_t* ev_do = ev + 2 + B;       // dO of element b on the device
+  cudaEvent_t* ev_fwd = ev + 2 + 2 * B;  // o, lse of element b computed
+  cudaEvent_t* ev_bwd = ev + 2 + 3 * B;  // dq, dk, dv of element b computed
   const auto H2D = cudaMemcpyHostToDevice;
   const auto D2H = cudaMemcpyDeviceToHost;
 #define FA_CU(x) \
@@ -128,19 +131,22 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
     FA_CU(cudaMemcpyAsync(d_q + b * L.q, hq + b * L.q, L.q, H2D, P.in));
     FA_CU(cudaMemcpyAsync(d_k + b * L.kv, hk + b * L.kv, L.kv, H2D, P.in));
     FA_CU(cudaMemcpyAsync(d_v + b * L.kv, hv + b * L.kv, L.kv, H2D, P.in));
+    FA_CU(cudaEventRecord(ev_qkv[b], P.in));
     FA_CU(cudaMemcpyAsync(d_do + b * L.q, hdo + b * L.q, L.q, H2D, P.in));
-    FA_CU(cudaEventRecord(ev_in[b], P.in));
+    FA_CU(cudaEventRecord(ev_do[b], P.in));
   }
   for (int b = 0; b < B; ++b) {
-    FA_CU(cudaStreamWaitEvent(st, ev_in[b], 0));
+    FA_CU(cudaStreamWaitEvent(st, ev_qkv[b], 0));
     int r = fa_fwd(d_q + b * L.q, d_k + b * L.kv, d_v + b * L.kv, d_o + b * L.q,
                    reinterpret_cast<float*>(d_lse + b * L.lse), 1, Hq, Hkv, N, d, causal, scale, stream);
     if (r != FA_OK) return r;
+    FA_CU(cudaEventRecord(ev_fwd[b], st));
+    FA_CU(cudaStreamWaitEvent(st, ev_do[b], 0));
     r = fa_bwd(d_q + b * L.q, d_k + b * L.kv, d_v + b * L.kv, d_o + b * L.q, d_do + b * L.q,
                reinterpret_cast<const float*>(d_lse + b * L.lse), d_dq + b * L.q, d_dk + b * L.kv, d_dv + b * L.kv, d_ws,
                L.bwd, 1, Hq, Hkv, N, d, causal, scale, stream);
     if (r != FA_OK) return r;
-    FA_CU(cudaEventRecord(ev_comp[b], st));
+    FA_CU(cudaEventRecord(ev_bwd[b], st));
   }
   char* ho = static_cast<char*>(o);
   char* hl = reinterpret_cast<char*>(lse);
@@ -148,9 +154,10 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
   char* hdk = static_cast<char*>(dk);
   char* hdv = static_cast<char*>(dv);
   for (int b = 0; b < B; ++b) {
-    FA_CU(cudaStreamWaitEvent(P.out, ev_comp[b], 0));
+    FA_CU(cudaStreamWaitEvent(P.out, ev_fwd[b], 0));
     FA_CU(cudaMemcpyAsync(ho + b * L.q, d_o + b * L.q, L.q, D2H, P.out));
     FA_CU(cudaMemcpyAsync(hl + b * L.lse, d_lse + b * L.lse, L.lse, D2H, P.out));
+    FA_CU(cudaStreamWaitEvent(P.out, ev_bwd[b], 0));
     FA_CU(cudaMemcpyAsync(hdq + b * L.q, d_dq + b * L.q, L.q, D2H, P.out));
     FA_CU(cudaMemcpyAsync(hdk + b * L.kv, d_dk + b * L.kv, L.kv, D2H, P.out));
     FA_CU(cudaMemcpyAsync(hdv + b * L.kv, d_dv + b * L.kv, L.kv, D2H, P.out));
