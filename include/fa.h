@@ -248,6 +248,17 @@ int fa_softmax_rows(const float *x, float *p, float *lse, long long rows, int n,
  */
 int fa_check(fa_stream_t stream);
 
+/*
+ * Self-test of the device failure path (the pages have no counterpart). Launches one warp
+ * that waits, with the same bounded wait every pipeline wait of the kernels uses, on a
+ * barrier that nothing completes. After the wait's time limit (2 s) the warp records the
+ * timeout in the device status word, as a stuck kernel would, and the kernel returns, so the
+ * context stays usable. *result (a device int) receives 2 when the wait gave up and raised
+ * its abort flag (1 if it had completed, 3 otherwise). The following fa_check(stream) returns
+ * FA_ERR_TIMEOUT and clears the status. Argument errors: FA_ERR_INVALID for a null result.
+ */
+int fa_selftest_wait_timeout(int *result, fa_stream_t stream);
+
 /* Static, human-readable description of a status code. */
 const char *fa_strerror(int status);
 

@@ -7,6 +7,29 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+// One warp waits, with the kernels' own bounded wait, on an mbarrier that nothing arrives at:
+// the wait gives up after its time limit, raises the CTA abort flag and records the timeout
+// in the device status word, and the kernel returns.
+__global__ void __launch_bounds__(32) fa_selftest_wait_kernel(uint32_t* status, int* result) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ int abort_flag;
+  const uint32_t bar = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const Ctl ctl{&abort_flag, status};
+  const bool ok = mbar_wait_warp(bar, 0, ctl);
+  if (threadIdx.x == 0) *result = ok ? 1 : (abort_flag ? 2 : 3);
+}
+
+}  // namespace fa
 
 namespace {
 
@@ -360,6 +383,15 @@ int fa_softmax_rows(const float* x, float* p, float* lse, long long rows, int n,
   return fa::launch_softmax_rows(x, p, lse, rows, n, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
              : FA_ERR_LAUNCH;
+}
+
+int fa_selftest_wait_timeout(int* result, fa_stream_t stream) {
+  if (result == nullptr) return FA_ERR_INVALID;
+  uint32_t* status = nullptr;
+  int r = current_device(&status);
+  if (r != FA_OK) return r;
+  fa::fa_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status, result);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_check(fa_stream_t stream) {

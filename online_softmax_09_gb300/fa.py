@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_bwd_host_workspace_bytes.restype = ctypes.c_size_t
         L.fa_fwd_bwd_host.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _i, _i, _f, _vp, ctypes.c_size_t, _vp]
         L.fa_fwd_bwd_host.restype = _i
+        L.fa_selftest_wait_timeout.argtypes = [_vp, _vp]
+        L.fa_selftest_wait_timeout.restype = _i
         L.fa_softmax_rows.argtypes = [_vp, _vp, _vp, ctypes.c_longlong, _i, _vp]
         L.fa_softmax_rows.restype = _i
         L.fa_check.argtypes = [_vp]
@@ -284,6 +286,19 @@ def fwd_bwd_host(q, k, v, do, causal: bool = False, scale: float | None = None, 
     if r != FA_OK:
         raise FAError(r, "fa_fwd_bwd_host")
     return o, lse, dq, dk, dv
+
+
+def selftest_wait_timeout(device=None, stream=None) -> int:
+    """Run fa_selftest_wait_timeout: one warp waits on a barrier nothing completes until the
+    bounded wait gives up (2 s). Returns the kernel's result code (2: gave up and raised its
+    abort flag); the device status then holds the timeout, which check() reports."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    res = torch.zeros(1, dtype=torch.int32, device=dev)
+    r = lib().fa_selftest_wait_timeout(res.data_ptr(), _stream_handle(stream, dev))
+    if r != FA_OK:
+        raise FAError(r, "fa_selftest_wait_timeout")
+    (stream if stream is not None else torch.cuda.current_stream(dev)).synchronize()
+    return int(res.item())
 
 
 def softmax_rows(x, out=None, lse=None, with_lse: bool = True, stream=None):
