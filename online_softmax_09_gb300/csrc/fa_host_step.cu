@@ -4,10 +4,13 @@
 // The computation is fa_fwd followed by fa_bwd ("LLM Architecture Refresh [3]: Flash Attention
 // Is Exact", sections 4 and 8), run once per batch element on that element's slices of the
 // [B][H][N][d] tensors (contiguous in this layout). Three streams carry a software pipeline:
-//   input stream   copies q, k, v, then dO of element b+1 to the device,
-//   caller stream  runs the forward and backward kernels of element b,
-//   output stream  copies o, lse of element b once its forward is done, then dq, dk, dv once
-//                  its backward is,
+//   input stream    copies q, k, v, then dO of each element to the device,
+//   compute streams run the forward and backward kernels of even elements on the caller's
+//                   stream and of odd elements on a second stream, each with its own backward
+//                   workspace, so one element's kernels fill the SMs that the previous
+//                   element's longest key tiles leave idle at the end of its backward,
+//   output stream   copies o, lse of an element once its forward is done, then dq, dk, dv once
+//                   its backward is,
 // ordered by events (each element's forward waits only for q, k, v; its backward for dO). GB300's copy engines move host data at about
 // 200 GB/s per direction and both directions at once, so for large steps the copies hide behind
 // the kernels except for the first element's inputs and the last element's outputs.
@@ -25,7 +28,7 @@ namespace {
 
 struct HostPipe {
   bool ready = false;
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp = nullptr;
   std::vector<cudaEvent_t> ev;  // [0] start, [1] done, then 4 per batch element
 };
 HostPipe g_pipe[64];
@@ -46,8 +49,10 @@ bool step_layout(int B, int Hq, int Hkv, int N, int d, StepLayout* L) {
   L->kv = (size_t)Hkv * N * d * 2;
   L->lse = (size_t)Hq * N * 4;
   L->bwd = bwd;
-  // q, dO, o, dq: B * q each; k, v, dk, dv: B * kv each; lse: B * lse; one bwd workspace.
-  L->total = 4 * align256(B * L->q) + 4 * align256(B * L->kv) + align256(B * L->lse) + align256(bwd);
+  // q, dO, o, dq: B * q each; k, v, dk, dv: B * kv each; lse: B * lse; a backward workspace
+  // per compute stream.
+  L->total = 4 * align256(B * L->q) + 4 * align256(B * L->kv) + align256(B * L->lse) +
+             (B > 1 ? 2 : 1) * align256(bwd);
   return true;
 }
 
@@ -56,6 +61,7 @@ cudaEvent_t* pipe_events(int dev, int B) {
   if (!P.ready) {
     if (cudaStreamCreateWithFlags(&P.in, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
     if (cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithFlags(&P.comp, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
     P.ready = true;
   }
   while ((int)P.ev.size() < 2 + 4 * B) {
@@ -102,7 +108,9 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
   char* d_dq = take(B * L.q);
   char* d_dk = take(B * L.kv);
   char* d_dv = take(B * L.kv);
-  char* d_ws = take(L.bwd);
+  char* d_ws[2];
+  d_ws[0] = take(L.bwd);
+  d_ws[1] = B > 1 ? take(L.bwd) : d_ws[0];
 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_pipe_mutex);
@@ -123,6 +131,7 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
   FA_CU(cudaEventRecord(ev_start, st));
   FA_CU(cudaStreamWaitEvent(P.in, ev_start, 0));
   FA_CU(cudaStreamWaitEvent(P.out, ev_start, 0));
+  FA_CU(cudaStreamWaitEvent(P.comp, ev_start, 0));
   const char* hq = static_cast<const char*>(q);
   const char* hk = static_cast<const char*>(k);
   const char* hv = static_cast<const char*>(v);
@@ -136,17 +145,19 @@ int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dou
     FA_CU(cudaEventRecord(ev_do[b], P.in));
   }
   for (int b = 0; b < B; ++b) {
-    FA_CU(cudaStreamWaitEvent(st, ev_qkv[b], 0));
+    const cudaStream_t cs = (b & 1) ? P.comp : st;
+    const fa_stream_t cs_h = reinterpret_cast<fa_stream_t>(cs);
+    FA_CU(cudaStreamWaitEvent(cs, ev_qkv[b], 0));
     int r = fa_fwd(d_q + b * L.q, d_k + b * L.kv, d_v + b * L.kv, d_o + b * L.q,
-                   reinterpret_cast<float*>(d_lse + b * L.lse), 1, Hq, Hkv, N, d, causal, scale, stream);
+                   reinterpret_cast<float*>(d_lse + b * L.lse), 1, Hq, Hkv, N, d, causal, scale, cs_h);
     if (r != FA_OK) return r;
-    FA_CU(cudaEventRecord(ev_fwd[b], st));
-    FA_CU(cudaStreamWaitEvent(st, ev_do[b], 0));
+    FA_CU(cudaEventRecord(ev_fwd[b], cs));
+    FA_CU(cudaStreamWaitEvent(cs, ev_do[b], 0));
     r = fa_bwd(d_q + b * L.q, d_k + b * L.kv, d_v + b * L.kv, d_o + b * L.q, d_do + b * L.q,
-               reinterpret_cast<const float*>(d_lse + b * L.lse), d_dq + b * L.q, d_dk + b * L.kv, d_dv + b * L.kv, d_ws,
-               L.bwd, 1, Hq, Hkv, N, d, causal, scale, stream);
+               reinterpret_cast<const float*>(d_lse + b * L.lse), d_dq + b * L.q, d_dk + b * L.kv, d_dv + b * L.kv,
+               d_ws[b & 1], L.bwd, 1, Hq, Hkv, N, d, causal, scale, cs_h);
     if (r != FA_OK) return r;
-    FA_CU(cudaEventRecord(ev_bwd[b], st));
+    FA_CU(cudaEventRecord(ev_bwd[b], cs));
   }
   char* ho = static_cast<char*>(o);
   char* hl = reinterpret_cast<char*>(lse);

@@ -78,7 +78,8 @@ def test_host_step_workspace_and_argument_errors(L):
     a = lambda x: (x + 255) // 256 * 256
     B, Hq, Hkv, N, d = 2, 8, 2, 1000, 128
     q, kv, lse = Hq * N * d * 2, Hkv * N * d * 2, Hq * N * 4
-    want = 4 * a(B * q) + 4 * a(B * kv) + a(B * lse) + a(L.fa_bwd_workspace_bytes(1, Hq, Hkv, N, d))
+    # Device copies of the nine tensors, and a backward workspace for each of two compute streams.
+    want = 4 * a(B * q) + 4 * a(B * kv) + a(B * lse) + 2 * a(L.fa_bwd_workspace_bytes(1, Hq, Hkv, N, d))
     assert L.fa_fwd_bwd_host_workspace_bytes(B, Hq, Hkv, N, d) == want
     assert L.fa_fwd_bwd_host_workspace_bytes(B, 3, 2, N, d) == 0  # Hq % Hkv != 0
     assert L.fa_fwd_bwd_host_workspace_bytes(0, Hq, Hkv, N, d) == 0
