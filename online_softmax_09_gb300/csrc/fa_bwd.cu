@@ -386,6 +386,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Window: query q sees key j only if q - j < window; (i - n) * 128 + q - kr is q - j.
       const bool wmask = kWin && (i - n) * kTile + kTile - 1 >= p.window;
       const float* sl = reinterpret_cast<const float*>(stage_ptr(s) + L::kStL);
+      // Queries of this tile that see this key row: [q_lo, q_hi] (none for a key past N).
+      const int q_lo = !key_ok ? kTile : (diag ? kr : 0);
+      const int q_hi = wmask ? kr + p.window - 1 - (i - n) * kTile : kTile - 1;
+      const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < kTile - 1);  // warp-uniform
       if (!mbar_wait_warp(bar(L::bQFull + s), (it >> 1) & 1, ctl)) return false;
       if (!mbar_wait_warp(bar(L::bSFull), it & 1, ctl)) return false;
       tc_fence_after();
@@ -395,19 +399,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t sr[32];
         tmem_ld32(tS + lane_off + c * 32, sr);
         tmem_ld_wait(sr);
+        if (masked) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float pv[4];
+          for (int j = 0; j < 32; j += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float pv[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int q = c * 32 + j + t;
-            pv[t] = ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
-            if (!key_ok || (diag && q < kr) || (wmask && (i - n) * kTile + q - kr >= p.window)) pv[t] = 0.f;
+            for (int t = 0; t < 4; ++t) {
+              const int q = c * 32 + j + t;
+              pv[t] = (q < q_lo || q > q_hi) ? 0.f : ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
+            }
+            pk[cc][j / 2] = pack_bf16(pv[0], pv[1]);
+            pk[cc][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
           }
-          pk[cc][j / 2] = pack_bf16(pv[0], pv[1]);
-          pk[cc][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
+            pk[cc][j / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sr[j]), sl2, -l4.x)),
+                                      ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, -l4.y)));
+            pk[cc][j / 2 + 1] = pack_bf16(ex2(fmaf(__uint_as_float(sr[j + 2]), sl2, -l4.z)),
+                                          ex2(fmaf(__uint_as_float(sr[j + 3]), sl2, -l4.w)));
+          }
         }
         // P^T (bf16) of chunk c into columns [64 grp + 16 cc, +16): score columns this warp
         // has already read.
