@@ -146,8 +146,9 @@ int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, co
  * The three stages fa_bwd runs, exposed so that a caller can schedule or time them apart.
  * They must be called in this order on one stream with the same sizes and workspace;
  * fa_bwd(...) is exactly prepare, compute, finalize.
- *   fa_bwd_prepare : delta = rowsum(dout * o) and lse * log2(e) per query row into the
- *                    workspace, and zeroes the workspace's fp32 dQ accumulator
+ *   fa_bwd_prepare : -delta = -rowsum(dout * o) and -lse * log2(e) per query row into the
+ *                    workspace (negated for the compute kernel's packed arithmetic), and
+ *                    zeroes the workspace's fp32 dQ accumulator
  *                    (memory-bound: reads o, dout, lse).
  *   fa_bwd_compute : the recompute kernel: writes dk, dv and adds dQ contributions (before
  *                    the final scale) into the workspace accumulator (reads q, k, v, dout).

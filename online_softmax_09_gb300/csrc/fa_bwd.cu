@@ -8,8 +8,8 @@
 //   dS = P * (dP - delta), dQ = scale dS K, dK = scale dS^T Q.
 //
 // Three kernels on the caller's stream:
-//   1. preprocess: delta and LSE*log2(e) per query row (padded rows: 0 and +inf), and zeroes
-//      the fp32 dQ accumulator.                                               (HBM-bound)
+//   1. preprocess: -delta and -LSE*log2(e) per query row (padded rows: 0 and -inf), and
+//      zeroes the fp32 dQ accumulator.                                         (HBM-bound)
 //   2. main: one CTA per (batch, kv head, 128-key tile). It keeps K_n and V_n in shared
 //      memory and the dK, dV accumulators in TMEM, and loops over the G query heads of its
 //      group and their query tiles (causal: from the diagonal tile on). Per query tile i:
@@ -79,9 +79,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
   const unsigned group = ((TPR == 32) ? 0xffffffffu : ((1u << TPR) - 1u)) << (lane & ~(TPR - 1));
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(group, s, off);
-  if (part == 0) {
-    delta[r] = (n < N) ? s : 0.f;
-    lse2[r] = (n < N) ? lse[(size_t)bh * N + n] * kLog2e : INFINITY;
+  if (part == 0) {  // stored negated: the main kernel adds them with packed f32x2 arithmetic
+    delta[r] = (n < N) ? -s : 0.f;
+    lse2[r] = (n < N) ? -(lse[(size_t)bh * N + n] * kLog2e) : -INFINITY;
   }
 }
 
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
               const int q = c * 32 + j + t;
-              pv[t] = (q < q_lo || q > q_hi) ? 0.f : ex2(fmaf(__uint_as_float(sr[j + t]), sl2, -lv[t]));
+              pv[t] = (q < q_lo || q > q_hi) ? 0.f : ex2(fmaf(__uint_as_float(sr[j + t]), sl2, lv[t]));
             }
             pk[cc][j / 2] = pack_bf16(pv[0], pv[1]);
             pk[cc][j / 2 + 1] = pack_bf16(pv[2], pv[3]);
@@ -416,11 +416,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);
-            pk[cc][j / 2] = pack_bf16(ex2(fmaf(__uint_as_float(sr[j]), sl2, -l4.x)),
-                                      ex2(fmaf(__uint_as_float(sr[j + 1]), sl2, -l4.y)));
-            pk[cc][j / 2 + 1] = pack_bf16(ex2(fmaf(__uint_as_float(sr[j + 2]), sl2, -l4.z)),
-                                          ex2(fmaf(__uint_as_float(sr[j + 3]), sl2, -l4.w)));
+            const float4 l4 = *reinterpret_cast<const float4*>(sl + c * 32 + j);  // -LSE2
+            const float2 x01 = fma2(make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])),
+                                    make_float2(sl2, sl2), make_float2(l4.x, l4.y));
+            const float2 x23 = fma2(make_float2(__uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3])),
+                                    make_float2(sl2, sl2), make_float2(l4.z, l4.w));
+            pk[cc][j / 2] = pack_bf16(ex2(x01.x), ex2(x01.y));
+            pk[cc][j / 2 + 1] = pack_bf16(ex2(x23.x), ex2(x23.y));
           }
         }
         // P^T (bf16) of chunk c into columns [64 grp + 16 cc, +16): score columns this warp
@@ -451,13 +453,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t ds[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(sd + c * 32 + j);
+          const float4 d4 = *reinterpret_cast<const float4*>(sd + c * 32 + j);  // -delta
           const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[cc][j / 2]));
           const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[cc][j / 2 + 1]));
-          ds[j / 2] = pack_bf16(p01.x * (__uint_as_float(dr[j + 0]) - d4.x),
-                                p01.y * (__uint_as_float(dr[j + 1]) - d4.y));
-          ds[j / 2 + 1] = pack_bf16(p23.x * (__uint_as_float(dr[j + 2]) - d4.z),
-                                    p23.y * (__uint_as_float(dr[j + 3]) - d4.w));
+          const float2 s01 = mul2(add2(make_float2(__uint_as_float(dr[j]), __uint_as_float(dr[j + 1])),
+                                       make_float2(d4.x, d4.y)), p01);
+          const float2 s23 = mul2(add2(make_float2(__uint_as_float(dr[j + 2]), __uint_as_float(dr[j + 3])),
+                                       make_float2(d4.z, d4.w)), p23);
+          ds[j / 2] = pack_bf16(s01.x, s01.y);
+          ds[j / 2 + 1] = pack_bf16(s23.x, s23.y);
         }
         // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
         // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
