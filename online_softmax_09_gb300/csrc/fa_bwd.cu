@@ -148,6 +148,7 @@ struct BwdSmem {
     bDPFull,
     bPReady,
     bSmemDS,
+    bDVDone,  // dV_i has finished reading dO_i (whose slot then takes dS_i)
     bDQFull,
     bDQFree,
     bFinal,
@@ -226,6 +227,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bPReady), 256);
     mbar_init(bar(L::bSmemDS), 256);
     mbar_init(bar(L::bDQFull), 1);
+    mbar_init(bar(L::bDVDone), 1);
     mbar_init(bar(L::bDQFree), 128);
     mbar_init(bar(L::bFinal), 1);
     mbar_init(bar(L::bDrain), 1);
@@ -294,9 +296,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
-    // Per query tile i: dV += P_i^T dO_i, dP_i^T = V dO_i^T, S_{i+1}^T = K Q_{i+1}^T,
-    // dQ_i = dS_i K, dK += dS_i^T Q_i. The softmax warps compute dS_i while S_{i+1}^T runs and
-    // P_{i+1} while dQ and dK run; the dQ drain overlaps dK and the next dV.
+    // Per query tile i: dV += P_i^T dO_i, S_{i+1}^T = K Q_{i+1}^T, dQ_i = dS_i K,
+    // dK += dS_i^T Q_i, then dP_{i+1}^T = V dO_{i+1}^T. dP does not depend on P, so it is issued
+    // as soon as its TMEM columns are free (dQ_i drained), ahead of the P phase it will meet:
+    // the softmax warps then go from P_{i+1} straight to dS_{i+1}. The dQ drain overlaps dK.
     if (lane == 0) {
       constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
@@ -310,32 +313,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(bar(L::bSFull));
       };
-      bool ok = mbar_wait(bar(L::bKV), 0, ctl) && mbar_wait(bar(L::bQFull), 0, ctl);
-      if (ok) {
+      // dP^T_it = V_n dO_it^T into tdP, once dO_it has landed and dQ_{it-1} has been drained
+      // out of these columns.
+      auto issue_dp = [&](int it) -> bool {
+        if (!mbar_wait(bar(L::bDOFull + (it & 1)), (it >> 1) & 1, ctl)) return false;
+        if (it > 0 && !mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl)) return false;
         tc_fence_after();
-        issue_s(0);
-      }
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        const uint32_t sQ = stage(s) + L::kStQ;
-        const uint32_t sDO = stage(s) + L::kStDO;
-        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand)
-        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
-        if (!(ok = mbar_wait(bar(L::bDOFull + s), ph, ctl))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
-        // dP^T = V_n dO_i^T, once the previous dQ has been drained out of these columns.
-        if (it > 0 && !(ok = mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl))) break;
-        tc_fence_after();
+        const uint32_t sDO = stage(it & 1) + L::kStDO;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
         }
         mma_commit(bar(L::bDPFull));
+        return true;
+      };
+      bool ok = mbar_wait(bar(L::bKV), 0, ctl) && mbar_wait(bar(L::bQFull), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = n_iter > 0 && issue_dp(0);
+      }
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it & 1;
+        const uint32_t sQ = stage(s) + L::kStQ;
+        const uint32_t sDO = stage(s) + L::kStDO;
+        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand; dO_i waited for dP_i)
+        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tdV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
+        mma_commit(bar(L::bDVDone));
         // S^T of the next query tile (P_i^T in these columns was read by the dV MMA above).
         if (it + 1 < n_iter) {
           if (!(ok = mbar_wait(bar(L::bQFull + (s ^ 1)), ((it + 1) >> 1) & 1, ctl))) break;
@@ -360,6 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                  (it > 0 || kk > 0));
         }
         mma_commit(bar(L::bStageEmpty + s));
+        if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
       }
       if (ok) mma_commit(bar(L::bFinal));
       if (*abort_flag) {
@@ -441,8 +451,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), (it >> 1) & 1, ctl))) break;
       if (!(ok = mbar_wait_warp(bar(L::bDPFull), it & 1, ctl))) break;
       tc_fence_after();
-      // dS^T = P^T (dP^T - delta) with the bf16 P the dV MMA used. dP_it^T being complete
-      // implies every earlier MMA is, so the dO slot (or the dS buffer) is free to overwrite.
+      // dS^T = P^T (dP^T - delta) with the bf16 P the dV MMA used. dS goes to shared memory
+      // only after dV_it (issued after dP_it) has read the dO slot it reuses (d = 128), and
+      // after dK_{it-2}, dQ_{it-2} -- the previous readers of this stage -- which the stage's
+      // reload for dO_it already implies.
       const uint32_t row_base = sDS(s) + (uint32_t)kr * 128;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -463,6 +475,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds[j / 2] = pack_bf16(s01.x, s01.y);
           ds[j / 2 + 1] = pack_bf16(s23.x, s23.y);
         }
+        // dS takes dO_it's slot (d = 128): dV_it, issued after dP_it, must have read it.
+        if (cc == 0 && !(ok = mbar_wait_warp(bar(L::bDVDone), it & 1, ctl))) break;
         // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
         // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
 #pragma unroll
@@ -472,6 +486,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        ds[4 * g4 + 2], ds[4 * g4 + 3]);
         }
       }
+      if (!ok) break;
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar(L::bSmemDS));
