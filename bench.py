@@ -14,6 +14,9 @@ runs the same per-GPU workload on its own GPU with no data-path collective (weak
 the timing uses a barrier and the max over ranks. `--impl reference` times the fp64 CPU
 oracle on the host cores on bounded samples of the same workload.
 `--batch B` shrinks the batch for profiling runs only; such a line is not a bench value.
+`--workload softmax_rows|splitkv|window|naive|sweep` times one of the extra workloads instead
+(the row softmax, split-KV, sliding window, S/P-through-HBM attention, and a sequence-length
+sweep at B*N = 16384) and prints its own JSON line.
 """
 
 from __future__ import annotations
@@ -549,6 +552,89 @@ def run_naive(args):
         "rows": rows}), flush=True)
 
 
+def _median_ms_cold(fn, steps, warmup, flush):
+    """Median over `steps` single calls of `fn`, each timed alone with CUDA events after a write
+    of `flush` (larger than L2), so that every call starts with its inputs in HBM only."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return statistics.median(times)
+
+
+def run_sweep(args):
+    """Sequence-length sweep at a fixed token count: B*N = 16384, Hq = Hkv = 16, N = 512..16384,
+    d in {64, 128}, causal and non-causal, inputs N(0,1) from seed 3. Per shape: forward,
+    backward (all three stages) and forward+backward step, each the median of single calls
+    with L2 flushed before each; TFLOP/s from algorithmic FLOPs and HBM GB/s from the
+    compulsory bytes (forward: read Q, K, V, write O and LSE; backward: read Q, K, V, O, dO and
+    LSE, write dQ, dK, dV)."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    burst, _, peak_src = load_peaks()
+    hbm, hbm_src = load_hbm_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    H, rows = 16, []
+    for d in (64, 128):
+        for N in (512, 1024, 2048, 4096, 8192, 16384):
+            B = 16384 // N
+            q, k, v, do = (t.cuda() for t in make_qkv(B, H, H, N, d, seed=3, with_do=True))
+            o = torch.empty_like(q)
+            lse = torch.empty(B, H, N, device=q.device)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(fa.workspace_bytes(B, H, H, N, d), dtype=torch.uint8, device=q.device)
+            tensor_bytes = B * H * N * d * 2
+            fwd_bytes = 4 * tensor_bytes + B * H * N * 4
+            bwd_bytes = 8 * tensor_bytes + B * H * N * 4
+            for causal in (False, True):
+                fl = fwd_flops(B, H, N, d, causal)
+
+                def fwd():
+                    fa.forward(q, k, v, causal, out=o, lse=lse)
+
+                def bwd():
+                    fa.backward(q, k, v, o, do, lse, causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+                def step():
+                    fwd()
+                    bwd()
+
+                t_f = _median_ms_cold(fwd, args.steps, args.warmup, flush)
+                t_b = _median_ms_cold(bwd, args.steps, args.warmup, flush)
+                t_s = _median_ms_cold(step, args.steps, args.warmup, flush)
+                fa.check()
+                rows.append({
+                    "d": d, "N": N, "B": B, "causal": causal,
+                    "fwd_ms": round(t_f, 4), "fwd_tflops": round(fl / (t_f * 1e-3) / 1e12, 1),
+                    "fwd_frac": round(fl / (t_f * 1e-3) / 1e12 / burst, 3),
+                    "fwd_hbm_gbs": round(fwd_bytes / (t_f * 1e-3) / 1e9, 1),
+                    "bwd_ms": round(t_b, 4), "bwd_tflops": round(BWD_FACTOR * fl / (t_b * 1e-3) / 1e12, 1),
+                    "bwd_hbm_gbs": round(bwd_bytes / (t_b * 1e-3) / 1e9, 1),
+                    "step_ms": round(t_s, 4), "step_tflops": round((1 + BWD_FACTOR) * fl / (t_s * 1e-3) / 1e12, 1)})
+            del q, k, v, do, o, lse, dq, dk, dv, ws
+    best = max(r["fwd_tflops"] for r in rows)
+    print(json.dumps({
+        "metric": "attention TFLOP/s over N at B*N=16384 (bf16, H=16, d=64/128, causal and non-causal)",
+        "value": best, "unit": "TFLOP/s (best forward in the sweep)", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "fa_fwd / fa_bwd sweep, B*N=16384, Hq=Hkv=16", "l2": "flushed before each call",
+                   "timing": "median of single calls"},
+        "peaks": {"bf16_tflops_burst": burst, "bf16_src": peak_src, "hbm_gbs": hbm, "hbm_src": hbm_src},
+        "gpu_launches": len(rows) * (args.warmup + args.steps) * 8, "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,7 +645,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
-    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive"],
+    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep"],
                     default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
     args = ap.parse_args()
@@ -573,6 +659,8 @@ def main():
         run_window(args)
     elif args.workload == "naive":
         run_naive(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
