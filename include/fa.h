@@ -197,11 +197,14 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
  *   q, k, v, dout: host inputs, same layouts and types as fa_fwd / fa_bwd.
  *   o (bf16), lse (fp32), dq, dk, dv (bf16): host outputs, same layouts as there.
  *   workspace: device memory of at least fa_fwd_bwd_host_workspace_bytes(...) bytes, 256-byte
- *     aligned; it holds device copies of all nine tensors and two backward workspaces.
- * The work runs batch element by batch element: while the kernels of one element run, the
- * inputs of later elements are copied in and the outputs of earlier ones out; even elements
- * compute on `stream`, odd ones on a second compute stream so that consecutive elements'
- * kernels overlap. The library creates its three streams once per device. Host buffers must be page-locked (pinned)
+ *     aligned; it holds device copies of all nine tensors and one backward workspace (sized
+ *     for one chunk) per compute stream.
+ * The work runs in chunks: each chunk is one batch element's slice of Hkv/s whole kv heads and
+ * the query heads that read them, s the smallest divisor of Hkv with B*s >= 8 (or Hkv). While
+ * the kernels of some chunks run, the inputs of later chunks are copied in and the outputs of
+ * earlier ones out. Chunk c computes on compute stream c mod min(B*s, 4), stream 0 being
+ * `stream`, so that several chunks' kernels share the GPU.
+ * The library creates its six streams once per device. Host buffers must be page-locked (pinned)
  * for the copies to overlap; pageable buffers give correct results without the overlap. The
  * call is asynchronous like the others: the outputs are complete once `stream` has passed this
  * call (e.g. after fa_check(stream)), and the call starts after everything enqueued on `stream`

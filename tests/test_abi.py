@@ -74,13 +74,30 @@ def test_workspace_size_is_linear_in_n(L):
     assert L.fa_bwd(*args, 0x1001, 1 << 30, 1, 1, 1, 128, 128, 0, 0.0, None) == -3
 
 
-def test_host_step_workspace_and_argument_errors(L):
+def _host_step_bytes(L, B, Hq, Hkv, N, d):
+    """The documented layout: each batch element in s chunks of Hkv/s kv heads (s the smallest
+    divisor of Hkv with B*s >= 8, else Hkv); device copies of the nine tensors, each chunk's lse
+    from a 256-byte boundary, and one chunk-sized backward workspace per compute stream
+    (min(B*s, 4) streams)."""
     a = lambda x: (x + 255) // 256 * 256
+    s = next((s for s in range(1, Hkv + 1) if Hkv % s == 0 and B * s >= 8), Hkv)
+    nkv = Hkv // s
+    nq = nkv * (Hq // Hkv)
+    q, kv = B * Hq * N * d * 2, B * Hkv * N * d * 2
+    return (4 * a(q) + 4 * a(kv) + B * s * a(nq * N * 4)
+            + min(B * s, 4) * a(L.fa_bwd_workspace_bytes(1, nq, nkv, N, d)))
+
+
+def test_host_step_workspace_and_argument_errors(L):
     B, Hq, Hkv, N, d = 2, 8, 2, 1000, 128
-    q, kv, lse = Hq * N * d * 2, Hkv * N * d * 2, Hq * N * 4
-    # Device copies of the nine tensors, and a backward workspace for each of two compute streams.
-    want = 4 * a(B * q) + 4 * a(B * kv) + a(B * lse) + 2 * a(L.fa_bwd_workspace_bytes(1, Hq, Hkv, N, d))
-    assert L.fa_fwd_bwd_host_workspace_bytes(B, Hq, Hkv, N, d) == want
+    for shape in [(B, Hq, Hkv, N, d), (4, 32, 8, 4096, 128), (1, 32, 8, 4096, 128), (16, 16, 16, 1024, 64),
+                  (1, 1, 1, 128, 128), (3, 6, 3, 333, 64), (2, 3, 1, 129, 64), (5, 8, 4, 77, 128)]:
+        assert L.fa_fwd_bwd_host_workspace_bytes(*shape) == _host_step_bytes(L, *shape), shape
+    # The Llama-3.1-8B shape: each batch element in 2 chunks of four kv heads (16 query heads);
+    # the nine tensors (all sizes multiples of 256 B) plus 4 chunk-sized workspaces.
+    tensors = 4 * (4 * 32 * 4096 * 128 * 2) + 4 * (4 * 8 * 4096 * 128 * 2) + 4 * 32 * 4096 * 4
+    assert L.fa_fwd_bwd_host_workspace_bytes(4, 32, 8, 4096, 128) == tensors + 4 * L.fa_bwd_workspace_bytes(
+        1, 16, 4, 4096, 128)
     assert L.fa_fwd_bwd_host_workspace_bytes(B, 3, 2, N, d) == 0  # Hq % Hkv != 0
     assert L.fa_fwd_bwd_host_workspace_bytes(0, Hq, Hkv, N, d) == 0
     ptrs = [0x1000] * 9

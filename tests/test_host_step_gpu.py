@@ -28,7 +28,10 @@ def _device_path(fa, q, k, v, do, causal):
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", [(3, 8, 2, 1000, 128, True), (2, 4, 4, 300, 64, False),
-                                                (1, 2, 1, 129, 128, True), (4, 4, 1, 512, 64, True)])
+                                                (1, 2, 1, 129, 128, True), (4, 4, 1, 512, 64, True),
+                                                # Chunks whose lse slices start off a 16-byte boundary.
+                                                (2, 3, 1, 129, 64, True), (1, 4, 2, 129, 128, False),
+                                                (3, 6, 3, 77, 128, True)])
 def test_matches_device_path(B, Hq, Hkv, N, d, causal):
     fa = fa_mod()
     q, k, v, do = make_qkv(B, Hq, Hkv, N, d, seed=6000 + N + d, value_scale=0.5, with_do=True)
