@@ -81,3 +81,18 @@ def test_workspace_errors():
         fa.fwd_bwd_host(q, k, v, do, True, workspace=small)
     with pytest.raises(ValueError):
         fa.fwd_bwd_host(q.cuda(), k, v, do, True)
+
+
+def test_full_size_bench_workload_matches_device_path():
+    # The shape and inputs the end-to-end benchmark times: B=4, Hq=32, Hkv=8, N=4096, d=128,
+    # causal, N(0,1)*0.5 from seed 2 (two chunks of four kv heads per batch element).
+    fa = fa_mod()
+    B, Hq, Hkv, N, d = 4, 32, 8, 4096, 128
+    q, k, v, do = (t.pin_memory() for t in make_qkv(B, Hq, Hkv, N, d, seed=2, value_scale=0.5, with_do=True))
+    got = fa.fwd_bwd_host(q, k, v, do, True)
+    fa.check()
+    ref = _device_path(fa, q, k, v, do, True)
+    for name, g, r in zip(("o", "lse", "dk", "dv"), (got[0], got[1], got[3], got[4]), (ref[0], ref[1], ref[3], ref[4])):
+        assert torch.equal(g, r), name
+    dq_err = float((got[2].float() - ref[2].float()).norm() / ref[2].float().norm())
+    assert dq_err <= 1e-3, dq_err
