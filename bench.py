@@ -342,7 +342,55 @@ def cpu_baseline(qh, kh, vh, doh, budget_s=15.0, rows_per_block=256):
     return {"value": round(done_flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": cores_used(),
             "kind": "oracle",
             "sample": f"fp64 NumPy oracle (S and P materialised), fwd+bwd of {done_rows} query rows starting at "
-                      f"head (0,0), {rows_per_block}-row blocks from the last row down, {t_used:.1f} s of host time"}
+                      f"head (0,0), {rows_per_block}-row blocks from the last row down, {t_used:.1f} s of host time",
+            "small_configs": small_config_timings()}
+
+
+SMALL_CONFIGS = [  # (name, B, H, N, d, causal, with backward, seed): the two small workload configurations
+    ("B=1 H=1 N=256 d=64 non-causal fwd", 1, 1, 256, 64, False, False, 0),
+    ("B=2 H=8 N=1024 d=64 causal fwd+bwd", 2, 8, 1024, 64, True, True, 1),
+    ("B=2 H=8 N=1024 d=64 non-causal fwd+bwd", 2, 8, 1024, 64, False, True, 1),
+]
+THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _time_small_configs(repeats=3):
+    """Best-of-`repeats` seconds of the fp64 oracle on each small configuration (whole problem)."""
+    import oracle
+    from online_softmax_09_gb300.inputs import make_qkv, to_f64
+
+    out = []
+    for name, B, H, N, d, causal, bwd, seed in SMALL_CONFIGS:
+        q, k, v, do = (to_f64(t) for t in make_qkv(B, H, H, N, d, seed=seed, with_do=True))
+        scale = 1 / math.sqrt(d)
+        best = float("inf")
+        for _ in range(repeats):
+            t = time.perf_counter()
+            oracle.attention_forward(q, k, v, causal, scale)
+            if bwd:
+                oracle.attention_backward(q, k, v, do, causal, scale)
+            best = min(best, time.perf_counter() - t)
+        out.append({"config": name, "seconds": round(best, 5)})
+    return out
+
+
+def small_config_timings():
+    """The oracle on the small configurations with all host cores, and with one thread (a child
+    process started with the BLAS thread variables set to 1, so the setting holds from import)."""
+    rows = _time_small_configs()
+    env = dict(os.environ, **{v: "1" for v in THREAD_VARS})
+    single = None
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--small-configs-child"], env=env,
+                           capture_output=True, text=True, timeout=300)
+        if r.returncode == 0:
+            single = json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.TimeoutExpired, ValueError, IndexError):
+        single = None
+    for i, row in enumerate(rows):
+        row["seconds_all_cores"] = row.pop("seconds")
+        row["seconds_1_thread"] = single[i]["seconds"] if single else None
+    return {"cores": cores_used(), "rows": rows}
 
 
 def run_reference(args):
@@ -648,7 +696,11 @@ def main():
     ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep"],
                     default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
+    ap.add_argument("--small-configs-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.small_configs_child:
+        print(json.dumps(_time_small_configs()), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.workload == "softmax_rows":

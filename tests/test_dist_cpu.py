@@ -65,3 +65,28 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     bench.run_reference(Args())  # returns at once: no work, no output on ranks other than 0
     assert capsys.readouterr().out == ""
+
+
+def test_small_config_oracle_timings(monkeypatch):
+    # The cpu_baseline leg times the oracle on the small configurations with all cores and, in
+    # a child process with the BLAS thread variables set to 1, with one thread.
+    import subprocess
+    import json
+
+    import bench
+
+    monkeypatch.setattr(bench, "SMALL_CONFIGS", bench.SMALL_CONFIGS[:1])
+    rows = bench._time_small_configs(repeats=1)
+    assert [r["config"] for r in rows] == ["B=1 H=1 N=256 d=64 non-causal fwd"] and rows[0]["seconds"] > 0
+
+    seen = {}
+
+    def fake_run(cmd, env, **kw):
+        seen["cmd"], seen["env"] = cmd, env
+        return subprocess.CompletedProcess(cmd, 0, stdout=json.dumps([{"config": "x", "seconds": 0.5}]) + "\n")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+    out = bench.small_config_timings()
+    assert seen["cmd"][-1] == "--small-configs-child"
+    assert all(seen["env"][v] == "1" for v in bench.THREAD_VARS)
+    assert out["rows"][0]["seconds_1_thread"] == 0.5 and out["rows"][0]["seconds_all_cores"] > 0
