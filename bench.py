@@ -507,30 +507,41 @@ def _time_ms(fn, steps, warmup):
 
 
 def run_splitkv(args):
-    """Split-KV forward on a small-batch shape whose plain grid leaves SMs idle: B=1, Hq=Hkv=8,
-    N=2048, d=128, causal (8 heads x 8 query-tile pairs = 64 work items for 152 SMs)."""
+    """Split-KV forward against the plain forward on small-batch shapes whose plain grid leaves
+    SMs idle or whose longest causal work item runs alone: B=1, Hq=Hkv, d=128; the headline shape
+    is H=8, N=2048, causal (8 heads x 8 query-tile pairs = 64 work items for 152 SMs)."""
     import torch
 
     from online_softmax_09_gb300 import fa
     from online_softmax_09_gb300.inputs import make_qkv
 
-    B, H, N, d = 1, 8, 2048, 128
-    q, k, v, _ = (t.cuda() if t is not None else None for t in make_qkv(B, H, H, N, d, seed=5, value_scale=0.5))
-    o = torch.empty_like(q)
-    lse = torch.empty(B, H, N, device=q.device)
-    ws = torch.empty(fa.lib().fa_fwd_splitkv_workspace_bytes(B, H, H, N, d, 16), dtype=torch.uint8, device=q.device)
-    fl = fwd_flops(B, H, N, d, True)
-    t_plain = _time_ms(lambda: fa.forward(q, k, v, True, out=o, lse=lse), args.steps, args.warmup)
-    t_split = _time_ms(lambda: fa.forward_splitkv(q, k, v, True, 0, out=o, lse=lse, workspace=ws), args.steps,
-                       args.warmup)
-    fa.check()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = []
+    for H, N, causal in ((8, 2048, True), (2, 8192, True), (4, 4096, True), (8, 2048, False), (16, 1024, True)):
+        B, d = 1, 128
+        q, k, v, _ = (t.cuda() if t is not None else None for t in make_qkv(B, H, H, N, d, seed=5, value_scale=0.5))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, device=q.device)
+        s = fa.splitkv_auto(B, H, H, N, d, causal, sms)
+        ws = torch.empty(max(16, fa.lib().fa_fwd_splitkv_workspace_bytes(B, H, H, N, d, s)), dtype=torch.uint8,
+                         device=q.device)
+        fl = fwd_flops(B, H, N, d, causal)
+        t_plain = _time_ms(lambda: fa.forward(q, k, v, causal, out=o, lse=lse), args.steps, args.warmup)
+        t_split = _time_ms(lambda: fa.forward_splitkv(q, k, v, causal, 0, out=o, lse=lse, workspace=ws),
+                           args.steps, args.warmup)
+        fa.check()
+        rows.append({"H": H, "N": N, "causal": causal, "splits": s, "plain_ms": round(t_plain, 4),
+                     "split_ms": round(t_split, 4), "split_tflops": round(fl / (t_split * 1e-3) / 1e12, 2),
+                     "speedup_vs_plain": round(t_plain / t_split, 3)})
+    r0 = rows[0]
     print(json.dumps({
         "metric": "split-KV forward TFLOP/s (bf16, B=1 H=8 N=2048 d=128 causal)",
-        "value": round(fl / (t_split * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(t_split, 4), "higher_is_better": True, "dtype": "bf16",
-        "data": "synthetic", "config": {"workload": "fa_fwd_splitkv (automatic split count) vs fa_fwd"},
-        "plain_fwd": {"tflops": round(fl / (t_plain * 1e-3) / 1e12, 2), "ms": round(t_plain, 4)},
-        "speedup_vs_plain": round(t_plain / t_split, 3), "gpu_launches": 2 * args.steps}), flush=True)
+        "value": r0["split_tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r0["split_ms"], "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": "fa_fwd_splitkv (automatic split count) vs fa_fwd, B=1 d=128"},
+        "speedup_vs_plain": r0["speedup_vs_plain"], "rows": rows,
+        "gpu_launches": sum(1 + (2 if r["splits"] > 1 else 1) for r in rows) * (args.steps + args.warmup)}),
+        flush=True)
 
 
 def run_window(args):

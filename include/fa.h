@@ -87,12 +87,21 @@ int fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *l
  * Refresh [3]", section 3): with w_s = exp(LSE_s - max_s LSE_s),
  * O = sum_s w_s O_s / sum_s w_s and LSE = max_s LSE_s + ln(sum_s w_s). Fills the GPU when
  * B * Hq * ceil(N / 256) is below the SM count.
- *   num_splits : 1..64, or <= 0 to let the library choose (it picks 1 when the GPU is full).
+ *   num_splits : 1..64, or <= 0 to let the library choose: fa_fwd_splitkv_auto's count for the
+ *                current device (1 unless splitting is predicted to save 10 % or more).
  *   workspace  : device, 16-byte aligned, >= fa_fwd_splitkv_workspace_bytes() bytes for the
  *                splits used (unused when 1 split is used); contents on entry do not matter.
  * Same outputs and errors as fa_fwd; FA_ERR_WORKSPACE if the workspace is too small.
  */
 size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int num_splits);
+/*
+ * The split count fa_fwd_splitkv uses for num_splits <= 0 on a GPU with num_sms SMs: the count
+ * in {1, 2, 4, 8, 16} with the least time predicted by a cost model of the persistent forward
+ * (its longest work item against its work per SM, in key-tile steps) plus the merge and the
+ * partial outputs' traffic, chosen only for a predicted gain of 10 % or more. Host-only, needs no
+ * GPU. Returns FA_ERR_INVALID (< 0) for invalid sizes or num_sms < 1.
+ */
+int fa_fwd_splitkv_auto(int B, int Hq, int Hkv, int N, int d, int causal, int num_sms);
 int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                    int B, int Hq, int Hkv, int N, int d, int causal, float scale, int num_splits,
                    void *workspace, size_t workspace_bytes, fa_stream_t stream);

@@ -1,6 +1,7 @@
 // fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA descriptors, launch.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -161,14 +162,50 @@ size_t splitkv_bytes(int B, int Hq, int N, int d, int splits, size_t* lse_off) {
   return o_bytes + (rows * 4 + 255) / 256 * 256;
 }
 
-// Splits used when the caller asks for automatic selection: enough work items to give every SM
-// one (counting the longest pair), at most 16, and at least 2 key tiles per split.
-int auto_splits(int B, int Hq, int N, int num_sms) {
+// Split count for automatic selection: the s in {1, 2, 4, 8, 16} with the least predicted time,
+// taken only for a predicted gain of 10 % or more over no split. The persistent forward takes the
+// longer of its longest work item and its work per SM, counted in key-tile steps of a two-tile
+// item (about 1.9 us at d = 128 and 1.6 us at d = 64, measured on GB300); a split adds the merge
+// kernel (about 5 us) and the fp32 partial outputs of every query tile that has more than one
+// non-empty split, written and read back (about 5 TB/s). Fitted to measured times of 1 to 16
+// splits on small-batch shapes, which it predicts within about 10 %.
+int auto_splits(int B, int Hq, int N, int d, int causal, int num_sms) {
   const int T = (N + fa::kTile - 1) / fa::kTile;
-  const long long items = (long long)((T + 1) / 2) * B * Hq;
-  int s = 1;
-  while (s < 16 && items * s < num_sms && T / (2 * s) >= 2) s *= 2;
-  return s;
+  const int pairs = (T + 1) / 2;
+  const double step_us = d == 128 ? 1.9 : 1.6;
+  const double heads = (double)B * Hq;
+  const double sms = num_sms > 0 ? num_sms : 1;
+  double t_plain = 0.0, t_best = 0.0;
+  int best = 1;
+  for (int s = 1; s <= 16 && s <= T; s *= 2) {
+    const int len = (T + s - 1) / s;
+    double longest = 0.0, work = 0.0;
+    for (int pr = 0; pr < pairs; ++pr) {
+      const int hi = causal ? std::min(2 * pr + 2, T) : T;  // key tiles of the pair's upper query tile
+      for (int sp = 0; sp * len < hi; ++sp) {
+        const int steps = std::min(hi, (sp + 1) * len) - sp * len;
+        longest = std::max(longest, (double)steps);
+        work += steps;
+      }
+    }
+    double t = std::max(longest, work * heads / sms) * step_us;
+    if (s > 1) {
+      double part_bytes = 0.0;  // per head
+      for (int qt = 0; qt < T; ++qt) {
+        const int hi = causal ? qt + 1 : T;
+        const int ns = std::min(s, (hi + len - 1) / len);
+        if (ns > 1) part_bytes += (double)ns * fa::kTile * d * 4;
+      }
+      t += 5.0 + 2.0 * part_bytes * heads / 5.0e6;
+    }
+    if (s == 1) {
+      t_plain = t_best = t;
+    } else if (t < 0.9 * t_plain && t < t_best) {
+      best = s;
+      t_best = t;
+    }
+  }
+  return best;
 }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
@@ -303,7 +340,7 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   if (num_splits <= 0) {
     int sms = 0;
     FA_TRY(current_device(nullptr, &sms));
-    num_splits = auto_splits(B, Hq, N, sms);
+    num_splits = auto_splits(B, Hq, N, d, causal, sms);
   }
   size_t lse_off = 0;
   const size_t need = splitkv_bytes(B, Hq, N, d, num_splits, &lse_off);
@@ -315,6 +352,12 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream, 0, num_splits,
                   num_splits > 1 ? reinterpret_cast<float*>(ws) : nullptr,
                   num_splits > 1 ? reinterpret_cast<float*>(ws + lse_off) : nullptr);
+}
+
+int fa_fwd_splitkv_auto(int B, int Hq, int Hkv, int N, int d, int causal, int num_sms) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  if (num_sms < 1) return FA_ERR_INVALID;
+  return auto_splits(B, Hq, N, d, causal, num_sms);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {

@@ -35,10 +35,6 @@
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
-// The split-KV instantiation ends its epilogue early; the plain epilogue after it is then
-// unreachable there by design.
-#pragma nv_diag_suppress 128
-
 namespace fa {
 
 struct FwdParams {
@@ -76,6 +72,13 @@ __device__ __forceinline__ int fwd_item_index(int r, int num_items) {
   const int G = gridDim.x;
   const int k = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
   return k < num_items ? k : -1;
+}
+
+// Splits that hold key tiles for query tile qt: the first ceil(hi / split_len) of them, hi being
+// the tile's end of visible keys (the diagonal when causal). Split mode has no window.
+__host__ __device__ __forceinline__ int split_count(int qt, const FwdParams& p) {
+  const int hi = p.causal ? qt + 1 : p.num_tiles;
+  return min(p.num_splits, (hi + p.split_len - 1) / p.split_len);
 }
 
 template <bool kWin, bool kSplit>
@@ -394,16 +397,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int a_t = t ? itm.a[1] : itm.a[0];
       const int n_kv = (t ? itm.b[1] : itm.b[0]) - a_t;
       const size_t part_row = ((size_t)itm.split * p.B * p.Hq + itm.bh) * p.N + row;
-      if (n_kv == 0) {
-        // This split has no key tile for this query tile: an empty partial (weight zero).
-        if (kSplit && row < p.N) {
-          p.lse_part[part_row] = -INFINITY;
-          float4* dst = reinterpret_cast<float4*>(p.o_part + part_row * D);
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        continue;
-      }
+      // This split has no key tile for this query tile: nothing to write, since the merge reads
+      // only the splits that hold keys for the tile.
+      if (n_kv == 0) continue;
       const int jbase = itm.j0 + a_t;  // absolute index of the first key tile
       float m_run = -INFINITY;  // reference max (base 2) of P, l and O
       float m_hi = -INFINITY;   // true running max (base 2)
@@ -506,8 +502,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       sc += n_kv;
       tc_fence_after();
       const float inv_l = 1.f / (l_run + e_run);
-      if (kSplit) {
-        // Split mode: the partial output acc / l (fp32) and its LSE, merged later.
+      if (kSplit && split_count(qt, p) > 1) {
+        // Split mode: the partial output acc / l (fp32) and its LSE, merged later. (A tile whose
+        // keys all fall in one split gets its final O and LSE below, as without splits.)
         if (row < p.N) p.lse_part[part_row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
         float4* dst = reinterpret_cast<float4*>(p.o_part + part_row * D);
 #pragma unroll
@@ -597,24 +594,25 @@ static cudaError_t launch_fwd_t(const FwdLaunch& a, const FwdParams& p) {
 
 // Split-KV merge ("LLM Architecture Refresh [3]", section 3, "Partial softmaxes compose"): per
 // row, O = sum_s w_s O_s / sum_s w_s and LSE = m + ln(sum_s w_s) with w_s = exp(LSE_s - m),
-// m = max_s LSE_s. One thread per 4 columns of a row.
+// m = max_s LSE_s, over the splits that hold keys for the row's tile. Rows whose keys all fall in
+// one split were written in full by the attention kernel. One thread per 4 columns of a row.
 template <int D>
 __global__ void __launch_bounds__(256) fa_split_merge_kernel(const float* __restrict__ o_part,
                                                             const float* __restrict__ lse_part,
                                                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                            long long rows, int num_splits) {
+                                                            long long rows, const FwdParams p) {
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gt / (D / 4);
   const int col = (int)(gt - row * (D / 4)) * 4;
   if (row >= rows) return;
+  const int ns = split_count((int)(row % p.N) / kTile, p);
+  if (ns <= 1) return;
   float m = -INFINITY;
-  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + row]);
+  for (int s = 0; s < ns; ++s) m = fmaxf(m, lse_part[(size_t)s * rows + row]);
   float wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < num_splits; ++s) {
-    const float ls = lse_part[(size_t)s * rows + row];
-    if (ls == -INFINITY) continue;  // empty partial
-    const float w = __expf(ls - m);
+  for (int s = 0; s < ns; ++s) {
+    const float w = __expf(lse_part[(size_t)s * rows + row] - m);
     const float4 v = *reinterpret_cast<const float4*>(o_part + ((size_t)s * rows + row) * D + col);
     acc.x += w * v.x;
     acc.y += w * v.y;
@@ -656,9 +654,9 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   const long long threads = rows * (a.d / 4);
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   if (a.d == 128)
-    fa_split_merge_kernel<128><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p.num_splits);
+    fa_split_merge_kernel<128><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p);
   else
-    fa_split_merge_kernel<64><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p.num_splits);
+    fa_split_merge_kernel<64><<<blocks, 256, 0, a.stream>>>(a.o_part, a.lse_part, p.o, a.lse, rows, p);
   return cudaGetLastError();
 }
 

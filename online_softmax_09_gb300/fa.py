@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_window.restype = _i
         L.fa_fwd_splitkv_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i]
         L.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_fwd_splitkv_auto.argtypes = [_i] * 7
+        L.fa_fwd_splitkv_auto.restype = _i
         L.fa_fwd_splitkv.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
                                      ctypes.c_size_t, _vp]
         L.fa_fwd_splitkv.restype = _i
@@ -141,7 +143,9 @@ def forward_splitkv(q, k, v, causal: bool = False, num_splits: int = 0, scale: f
     o = out if out is not None else torch.empty_like(q)
     l = lse if lse is not None else torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
     if workspace is None:
-        n = int(lib().fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, N, d, int(num_splits) if num_splits > 0 else 16))
+        used = int(num_splits) if num_splits > 0 else splitkv_auto(
+            B, Hq, Hkv, N, d, causal, torch.cuda.get_device_properties(q.device).multi_processor_count)
+        n = int(lib().fa_fwd_splitkv_workspace_bytes(B, Hq, Hkv, N, d, used))
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
     sc = 0.0 if scale is None else float(scale)
     r = lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
@@ -150,6 +154,14 @@ def forward_splitkv(q, k, v, causal: bool = False, num_splits: int = 0, scale: f
     if r != FA_OK:
         raise FAError(r, "fa_fwd_splitkv")
     return o, l
+
+
+def splitkv_auto(B: int, Hq: int, Hkv: int, N: int, d: int, causal: bool, num_sms: int) -> int:
+    """The split count fa_fwd_splitkv picks for num_splits <= 0 on a GPU with num_sms SMs."""
+    r = lib().fa_fwd_splitkv_auto(B, Hq, Hkv, N, d, int(bool(causal)), num_sms)
+    if r < 0:
+        raise FAError(r, "fa_fwd_splitkv_auto")
+    return r
 
 
 def forward_naive(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None,

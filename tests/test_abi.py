@@ -107,3 +107,19 @@ def test_host_step_workspace_and_argument_errors(L):
     assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 128, 0, 0.0, 0x1080, ws, None) == -3  # not 256-aligned
     assert L.fa_fwd_bwd_host(None, *ptrs[1:], 1, 1, 1, 128, 128, 0, 0.0, 0x1000, ws, None) == -1
     assert L.fa_fwd_bwd_host(*ptrs, 1, 1, 1, 128, 96, 0, 0.0, 0x1000, ws, None) == -1  # d = 96: no layout
+
+
+def test_splitkv_auto_choice(L):
+    # Host-only cost model: no split when the GPU is full or the work items are already short,
+    # a split when a few long causal items would otherwise run alone.
+    assert L.fa_fwd_splitkv_auto(4, 32, 8, 4096, 128, 1, 152) == 1   # 2048 work items
+    assert L.fa_fwd_splitkv_auto(1, 8, 8, 8192, 128, 1, 152) == 1    # enough work per SM already
+    assert L.fa_fwd_splitkv_auto(1, 16, 16, 1024, 128, 1, 152) == 1  # items of at most 8 key tiles
+    assert L.fa_fwd_splitkv_auto(1, 2, 2, 8192, 128, 1, 152) > 1     # 64 items, the longest 64 tiles
+    assert L.fa_fwd_splitkv_auto(1, 4, 4, 4096, 128, 1, 152) > 1
+    for shape in [(1, 1, 1, 1, 64, 0), (1, 2, 1, 300, 128, 1), (2, 4, 2, 131072, 64, 0)]:
+        assert 1 <= L.fa_fwd_splitkv_auto(*shape, 152) <= 16
+    assert L.fa_fwd_splitkv_auto(1, 2, 1, 300, 128, 1, 1) >= 1
+    assert L.fa_fwd_splitkv_auto(1, 3, 2, 300, 128, 1, 152) < 0      # Hq % Hkv != 0
+    assert L.fa_fwd_splitkv_auto(1, 2, 1, 300, 96, 1, 152) < 0       # d = 96
+    assert L.fa_fwd_splitkv_auto(1, 2, 1, 300, 128, 1, 0) < 0        # no SMs
