@@ -79,6 +79,12 @@ def test_splitkv_auto_and_matches_plain_forward():
     O_ref, L_ref = oracle.attention_forward(to_f64(q), to_f64(k), to_f64(v), True, 1 / math.sqrt(128))
     assert_fwd_close(o_s.float().cpu().numpy(), l_s.cpu().numpy(), O_ref, L_ref, "auto split")
     assert float((o_s.float() - o_p.float()).abs().max()) < 2e-2
+    # Query tiles whose visible keys all lie in the first split are finished by the attention
+    # kernel itself, over the same key tiles in the same order as without splits: bit-identical.
+    s = fa.splitkv_auto(1, 8, 8, 2048, 128, True, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert s > 1
+    rows = ((16 + s - 1) // s) * 128  # split_len key tiles, causal: query tiles below split_len
+    assert torch.equal(o_s[:, :, :rows], o_p[:, :, :rows]) and torch.equal(l_s[:, :, :rows], l_p[:, :, :rows])
 
 
 @pytest.mark.parametrize("N", [7, 300, 1024])
