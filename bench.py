@@ -202,6 +202,13 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     fa.check()
+    # Tiles the forward computes and skips (fa_fwd_stats, one counted call outside the timed
+    # region): the FLOPs the kernels execute, whole 128 x 128 tiles included.
+    counters = torch.zeros(3, dtype=torch.int64, device=dev)
+    fa.forward(q, k, v, causal, out=o, lse=lse, counters=counters)
+    fa.check()
+    tiles_done, tiles_skipped = (int(x) for x in counters[:2].tolist())
+    tile_fwd_flops = tiles_done * 4 * 128 * 128 * d
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
@@ -294,6 +301,11 @@ def run_ours(args):
                      "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step loop)",
                      "frac": round(achieved / sustained, 4), "traffic": measured_traffic(),
                      "algorithmic_flops_per_launch": f_fwd * BWD_FACTOR, "ms_per_launch": round(bwd_compute_ms, 4)},
+        "executed": {"tiles_computed": tiles_done, "tiles_skipped": tiles_skipped,
+                     "fwd_flops": tile_fwd_flops, "fwd_tflops": round(tile_fwd_flops / (fwd_ms * 1e-3) / 1e12, 2),
+                     "fwd_bwd_tflops": round(tile_fwd_flops * (1 + BWD_FACTOR) / (ms_step * 1e-3) / 1e12, 2),
+                     "note": "FLOPs of every computed 128x128 tile (diagonal tiles in full), against the "
+                             "algorithmic count of visible pairs used everywhere else"},
         "e2e": e2e,
         "gpu_launches": 4 * K,
         "clocks": clocks,
