@@ -267,7 +267,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   if (workspace == nullptr || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
   uint32_t* status = nullptr;
-  FA_TRY(current_device(&status));
+  int num_sms = 0;
+  FA_TRY(current_device(&status, &num_sms));
   char* ws = static_cast<char*>(workspace);
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (stages & fa::kBwdCompute) {
@@ -301,6 +302,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.d = d;
   a.causal = (causal || window > 0) ? 1 : 0;
   a.window = window;
+  a.num_sms = num_sms;
   a.scale = resolve_scale(scale, d);
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return fa::launch_bwd(a, stages) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

@@ -22,7 +22,9 @@
 //      The next tile's S^T is computed while the softmax warps work on dS_i, and its P while
 //      the dQ and dK MMAs run, so the tensor core does not wait for the softmax warps. The one
 //      shared-memory copy of dS serves both of its MMAs (MN-major A of dQ, K-major A of dK),
-//      and dQ goes first so that its drain overlaps the dK MMA.
+//      and dQ goes first so that its drain overlaps the dK MMA. CTAs are launched in bands of
+//      (batch, kv head) pairs, key tile by key tile within a band, so that the Q, dO and dQ
+//      accumulator rows that a band's CTAs share stay in L2 (see bwd_band).
 //   3. dQ conversion: dq = bf16(scale * accumulator).
 //
 // Warp roles of the main kernel: 0-3 and 10-13 softmax/dS (thread = key row; warps 0-3 take
@@ -34,6 +36,8 @@
 // [64, 128) in [64, 96), i.e. each half over score columns its own warps have already read.
 // For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
 // once the dV and dP MMAs (the readers of dO) have completed; for D = 64 it has its own buffer.
+#include <cmath>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -120,6 +124,7 @@ struct BwdParams {
   int B, Hq, Hkv, N, Npad, causal, num_tiles;
   int window;  // > 0: causal sliding window of this many keys
   float scale, scale_log2;
+  int band;  // (b, kv head) pairs per launch band; B * Hkv for a single band
 };
 
 template <int D>
@@ -196,10 +201,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: key tile n of kv head (b, hkv). Causal tiles with the most query tiles first.
+  // Work item: key tile n of kv head (b, hkv). CTAs are numbered band by band (p.band
+  // consecutive (b, kv head) pairs, the last band possibly narrower) and key tile by key tile
+  // within a band, so a band's causal tiles with the most query tiles start first and its
+  // Q, dO and dQ accumulator rows stay in L2 while its CTAs run.
   const int BHk = p.B * p.Hkv;
-  const int n = blockIdx.x / BHk;
-  const int bhk = blockIdx.x - n * BHk;
+  const int per_band = p.band * p.num_tiles;
+  const int band_i = blockIdx.x / per_band;
+  const int first = band_i * p.band;
+  const int width = min(p.band, BHk - first);
+  const int local = blockIdx.x - band_i * per_band;
+  const int n = local / width;
+  const int bhk = first + (local - n * width);
   const int b = bhk / p.Hkv;
   const int hkv = bhk - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
@@ -577,6 +590,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// (b, kv head) pairs per launch band. A band's working set (its G query heads' Q and dO, bf16,
+// and dQ accumulator, fp32, plus K and V) is kept within about 80 MiB of the 129 MB L2, and its
+// work per SM must be at least 1.4 times its longest CTA, whose G * T query tiles would
+// otherwise end alone (a measured margin: 1.28 lost 3 %, 1.41 and above gained). Where both
+// cannot hold (large heads or groups), or for the sliding window, one band: plain
+// key-tile-major order.
+static int bwd_band(int B, int Hq, int Hkv, int N, int d, int causal, int window, int num_sms) {
+  const int BHk = B * Hkv;
+  const int T = (N + kTile - 1) / kTile;
+  const int G = Hq / Hkv;
+  if (window > 0 || num_sms < 1) return BHk;
+  const double ws = (double)N * d * (8.0 * G + 4.0);
+  const int kb_l2 = (int)(80.0 * 1024.0 * 1024.0 / ws);
+  // Work of one (b, kv head) in query-tile iterations, over its longest CTA's: (T + 1) / 2
+  // causal, T non-causal.
+  const double ratio = causal ? (T + 1) / 2.0 : (double)T;
+  const int kb_tail = (int)std::ceil(1.4 * num_sms / ratio);
+  if (kb_l2 < kb_tail || kb_tail >= BHk) return BHk;
+  const int nb = (BHk + kb_l2 - 1) / kb_l2;
+  const int kb = (BHk + nb - 1) / nb;
+  return kb < kb_tail ? kb_tail : kb;
+}
+
 template <int D>
 static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
   const int T = (a.N + kTile - 1) / kTile;
@@ -614,6 +650,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     p.window = a.window;
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
+    p.band = bwd_band(a.B, a.Hq, a.Hkv, a.N, D, a.causal, a.window, a.num_sms);
     const long long grid = (long long)a.B * a.Hkv * T;
     kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, p);
     e = cudaGetLastError();

@@ -46,6 +46,7 @@ struct BwdLaunch {
   uint32_t* status;
   int B, Hq, Hkv, N, d, causal;
   int window;  // 0: none; > 0: causal sliding window
+  int num_sms;
   float scale;
   cudaStream_t stream;
 };
