@@ -36,6 +36,7 @@
 // [64, 128) in [64, 96), i.e. each half over score columns its own warps have already read.
 // For D = 128 the dS operand of the dQ MMA is written into the dO slot of the current stage
 // once the dV and dP MMAs (the readers of dO) have completed; for D = 64 it has its own buffer.
+#include <algorithm>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -590,27 +591,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// (b, kv head) pairs per launch band. A band's working set (its G query heads' Q and dO, bf16,
-// and dQ accumulator, fp32, plus K and V) is kept within about 80 MiB of the 129 MB L2, and its
-// work per SM must be at least 1.4 times its longest CTA, whose G * T query tiles would
-// otherwise end alone (a measured margin: 1.28 lost 3 %, 1.41 and above gained). Where both
-// cannot hold (large heads or groups), or for the sliding window, one band: plain
-// key-tile-major order.
+// (b, kv head) pairs per launch band. Bands shrink the set of heads whose Q, dO and fp32 dQ
+// accumulator rows the resident CTAs share: as many bands as keep each band's work per SM at
+// least 1.4 times its longest CTA (whose G * T query tiles would otherwise end alone; a
+// measured margin: 1.28 lost 3 %, 1.41 and above gained), but no more than it takes to fit a
+// band's working set (its G query heads' Q and dO, bf16, and dQ accumulator, fp32, plus K and
+// V) in about 80 MiB of the 129 MB L2. One band (plain key-tile-major order) where the margin
+// allows no split, and for the sliding window.
 static int bwd_band(int B, int Hq, int Hkv, int N, int d, int causal, int window, int num_sms) {
   const int BHk = B * Hkv;
   const int T = (N + kTile - 1) / kTile;
   const int G = Hq / Hkv;
   if (window > 0 || num_sms < 1) return BHk;
   const double ws = (double)N * d * (8.0 * G + 4.0);
-  const int kb_l2 = (int)(80.0 * 1024.0 * 1024.0 / ws);
+  const int kb_l2 = std::max(1, (int)(80.0 * 1024.0 * 1024.0 / ws));
   // Work of one (b, kv head) in query-tile iterations, over its longest CTA's: (T + 1) / 2
   // causal, T non-causal.
   const double ratio = causal ? (T + 1) / 2.0 : (double)T;
   const int kb_tail = (int)std::ceil(1.4 * num_sms / ratio);
-  if (kb_l2 < kb_tail || kb_tail >= BHk) return BHk;
-  const int nb = (BHk + kb_l2 - 1) / kb_l2;
-  const int kb = (BHk + nb - 1) / nb;
-  return kb < kb_tail ? kb_tail : kb;
+  if (kb_tail >= BHk) return BHk;
+  // As many bands as the tail margin allows, but no more than it takes to fit the L2 budget;
+  // fewer if the last (narrower) band would miss the margin.
+  const int nb_l2 = (BHk + kb_l2 - 1) / kb_l2;
+  for (int nb = std::min(nb_l2, BHk / kb_tail); nb > 1; --nb) {
+    const int kb = (BHk + nb - 1) / nb;
+    if (kb >= kb_tail && BHk - (nb - 1) * kb >= kb_tail) return kb;
+  }
+  return BHk;
 }
 
 template <int D>
