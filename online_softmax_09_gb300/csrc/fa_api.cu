@@ -314,17 +314,20 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
            int d, int causal, float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_fwd");
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, nullptr, stream);
 }
 
 int fa_fwd_stats(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                  int N, int d, int causal, float scale, unsigned long long* counters, fa_stream_t stream) {
+  fa::TraceRange trace("fa_fwd_stats");
   if (counters == nullptr) return FA_ERR_INVALID;
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, counters, stream);
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                   int d, int window, float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_fwd_window");
   if (window < 1) return FA_ERR_INVALID;
   return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, 1, scale, nullptr, stream, window);
 }
@@ -337,6 +340,7 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N,
                    int d, int causal, float scale, int num_splits, void* workspace, size_t workspace_bytes,
                    fa_stream_t stream) {
+  fa::TraceRange trace("fa_fwd_splitkv");
   FA_TRY(check_sizes(B, Hq, Hkv, N, d));
   if (num_splits > 64) return FA_ERR_INVALID;
   if (num_splits <= 0) {
@@ -370,6 +374,7 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
            int N, int d, int causal, float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd");
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, causal, scale,
                   stream, fa::kBwdAll);
 }
@@ -377,6 +382,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
                   int N, int d, int window, float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd_window");
   if (window < 1) return FA_ERR_INVALID;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d, 1, scale,
                   stream, fa::kBwdAll, window);
@@ -384,6 +390,7 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
 
 int fa_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace, size_t workspace_bytes,
                    int B, int Hq, int Hkv, int N, int d, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd_prepare");
   return bwd_impl(nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr, nullptr, workspace, workspace_bytes,
                   B, Hq, Hkv, N, d, 0, 0.f, stream, fa::kBwdPrepare);
 }
@@ -391,12 +398,14 @@ int fa_bwd_prepare(const void* o, const void* dout, const float* lse, void* work
 int fa_bwd_compute(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
                    void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal,
                    float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd_compute");
   return bwd_impl(q, k, v, nullptr, dout, nullptr, nullptr, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, N, d,
                   causal, scale, stream, fa::kBwdCompute);
 }
 
 int fa_bwd_finalize(void* dq, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d,
                     float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd_finalize");
   return bwd_impl(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr, workspace,
                   workspace_bytes, B, Hq, Hkv, N, d, 0, scale, stream, fa::kBwdFinalize);
 }
@@ -409,6 +418,7 @@ size_t fa_naive_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
 int fa_naive_fwd(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                  size_t workspace_bytes, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                  fa_stream_t stream) {
+  fa::TraceRange trace("fa_naive_fwd");
   FA_TRY(check_sizes(B, Hq, Hkv, N, d));
   for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)}) FA_TRY(check_ptr(p));
   if (workspace == nullptr || workspace_bytes < fa::naive_workspace_bytes(B, Hq, N)) return FA_ERR_WORKSPACE;
@@ -420,6 +430,7 @@ int fa_naive_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 }
 
 int fa_softmax_rows(const float* x, float* p, float* lse, long long rows, int n, fa_stream_t stream) {
+  fa::TraceRange trace("fa_softmax_rows");
   if (rows < 1 || rows > 0x7fffffffLL || n < 1) return FA_ERR_INVALID;
   FA_TRY(check_ptr(x));
   FA_TRY(check_ptr(p));

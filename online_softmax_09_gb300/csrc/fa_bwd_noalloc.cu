@@ -47,6 +47,7 @@ int scratch_on_current_device(void** addr) {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
                               int d, int causal, float scale, fa_stream_t stream) {
+  fa::TraceRange trace("fa_bwd_noalloc");
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Hkv, N, d);
   if (need > FA_BWD_NOALLOC_MAX_BYTES) return FA_ERR_WORKSPACE;  // too large for the fixed scratch
   void* scratch = nullptr;

@@ -118,6 +118,7 @@ size_t fa_fwd_bwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
 int fa_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout, void* o, float* lse, void* dq,
                     void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                     void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  fa::TraceRange trace("fa_fwd_bwd_host");
   StepLayout L;
   if (!step_layout(B, Hq, Hkv, N, d, &L)) return FA_ERR_INVALID;
   if (!q || !k || !v || !dout || !o || !lse || !dq || !dk || !dv) return FA_ERR_INVALID;

@@ -3,11 +3,21 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 namespace fa {
 
 constexpr int kTile = 128;  // query rows and key rows per tile (B_r = B_c = 128)
+
+// A named range on the host timeline around one library call (NVTX), for Nsight tools when one
+// is attached; without a tool each push and pop is a call that returns at once.
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
 
 struct FwdLaunch {
   const CUtensorMap* tm_q;
