@@ -109,17 +109,16 @@ size_t naive_workspace_bytes(int B, int Hq, int N) {
 // Returns 0, or 1 when cuBLAS cannot be loaded, or 2 on a cuBLAS / launch error.
 int launch_naive_fwd(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace, int B,
                      int Hq, int Hkv, int N, int d, int causal, float scale, cudaStream_t st) {
-  cublasHandle_t handle;
-  {
-    std::lock_guard<std::mutex> lock(g_cublas_mutex);
-    if (!load_cublas()) return 1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2;
-    if (g_cublas.handles[dev] == nullptr && g_cublas.create(&g_cublas.handles[dev]) != CUBLAS_STATUS_SUCCESS)
-      return 2;
-    handle = g_cublas.handles[dev];
-    if (g_cublas.set_stream(handle, st) != CUBLAS_STATUS_SUCCESS) return 2;
-  }
+  // One cuBLAS handle per device, shared by all callers: the lock covers setting its stream and
+  // every GEMM enqueued with it, so concurrent calls on other streams cannot redirect them.
+  std::lock_guard<std::mutex> lock(g_cublas_mutex);
+  if (!load_cublas()) return 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2;
+  if (g_cublas.handles[dev] == nullptr && g_cublas.create(&g_cublas.handles[dev]) != CUBLAS_STATUS_SUCCESS)
+    return 2;
+  cublasHandle_t handle = g_cublas.handles[dev];
+  if (g_cublas.set_stream(handle, st) != CUBLAS_STATUS_SUCCESS) return 2;
   const size_t nn = (size_t)N * N;
   float* S = static_cast<float*>(workspace);
   __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) +
