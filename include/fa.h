@@ -11,7 +11,7 @@
  * "LLM Architecture Refresh [3]: Flash Attention Is Exact", sections 2 and 4).
  * Key/value tiles lying wholly in a query tile's causal future are skipped, not masked
  * (same post, section 7). The backward pass recomputes P from Q, K, V and LSE instead
- * of storing it (same post, section 8, "One more piece: the backward pass").
+ * of storing it (same post, section 8, its paragraph on the backward pass).
  *
  * Layout. All tensors are dense, row-major and contiguous:
  *     q, o, dout, dq : [B][Hq ][N][d]   bfloat16 (2 bytes, IEEE bfloat16 bit pattern)

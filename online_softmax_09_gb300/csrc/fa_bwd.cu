@@ -2,7 +2,7 @@
 //
 // The forward pass kept only O and the per-row log-sum-exp; the probabilities are recomputed
 // tile by tile from Q, K, V and LSE instead of being stored ("LLM Architecture Refresh [3]:
-// Flash Attention Is Exact", section 8, "One more piece: the backward pass"). Gradients are
+// Flash Attention Is Exact", section 8, its paragraph on the backward pass). Gradients are
 // the textbook ones for O = softmax(scale Q K^T) V:
 //   P = exp(scale S - LSE), dV = P^T dO, dP = dO V^T, delta = rowsum(dO * O),
 //   dS = P * (dP - delta), dQ = scale dS K, dK = scale dS^T Q.

@@ -7,7 +7,8 @@ Conventions (the plainest reading where the pages leave a point open):
 
 * Tensors are ``[B, H, N, d]`` float64 arrays (the pages slice queries as
   ``q[:, :, i:i+block]``, [P3] section 4). Queries and keys have the same
-  length N ([P3] appendix, "n here is one length, not two").
+  length N ([P3] appendix: a single pass over one sequence, so the score
+  matrix is square).
 * Grouped-query attention: query head ``hq`` reads key/value head
   ``hq // G`` with ``G = Hq // Hkv`` (contiguous groups). The pages mention GQA
   only for Llama's head counts ([P3] section 6); this mapping is a reading.
@@ -15,7 +16,7 @@ Conventions (the plainest reading where the pages leave a point open):
   become minus infinity ([P3] section 5).
 * The per-row statistic saved for the backward pass is the natural-log
   log-sum-exp ``LSE_i = m_i + ln(l_i)`` of the scaled scores. [P3] section 8
-  says only "the saved statistics"; LSE is the one scalar that lets P be
+  mentions only statistics kept from the forward pass; LSE is the one scalar that lets P be
   recomputed as ``exp(S - LSE)``.
 """
 
@@ -145,8 +146,9 @@ def attention_rows(q_rows, k, v, rows, causal: bool, scale: float, window=None):
 def attention_backward_head(q, k, v, do, causal: bool, scale: float, window=None):
     """Gradients of standard attention for one head.
 
-    [P3] section 8 ("One more piece: the backward pass") says only that the
-    probabilities are recomputed from Q, K, V and the saved statistics. The
+    [P3] section 8 (its paragraph on the backward pass) says only that the
+    probabilities are recomputed from Q, K, V and statistics kept from the
+    forward pass. The
     gradient itself is the textbook one for ``O = softmax(scale Q K^T) V``:
     ``dV = P^T dO``; ``dP = dO V^T``; ``delta = rowsum(dO * O)``;
     ``dS = P * (dP - delta)``; ``dQ = scale dS K``; ``dK = scale dS^T Q``.
@@ -231,13 +233,23 @@ def brute_force_attention(q, k, v, causal: bool, scale: float, window=None):
 # --------------------------------------------------------------------------
 
 
+def _rebase(m_old, m_new):
+    """exp(m_old - m_new), taken as 0 where nothing has been seen yet (m_old = -inf)."""
+    seen = ~np.isneginf(m_old)
+    return np.where(seen, np.exp(np.where(seen, m_old - m_new, 0.0)), 0.0)
+
+
 def online_softmax(x, block_size: int):
     """Single-pass online normaliser over the last axis ([P3] section 2, [P1]).
 
-    Carries a running max ``m`` and running sum ``l``. For each block:
-    ``m_new = max(m_old, max(block))``; ``correction = exp(m_old - m_new)``;
-    ``l = l * correction + sum(exp(block - m_new))``.
-    A second pass then forms ``exp(x - m) / l``.
+    The row is cut into blocks of ``block_size`` values. Each block has its own
+    partial statistics, its maximum ``m_b`` and ``l_b = sum(exp(block - m_b))``;
+    they are merged into the running ``(m, l)`` by rebasing both to the larger
+    maximum ([P3] section 3, "Partial softmaxes compose"):
+    ``m_new = max(m, m_b)``, ``correction = exp(m - m_new)``,
+    ``l = l * correction + l_b * exp(m_b - m_new)`` -- the same running sum as
+    ``l * correction + sum(exp(block - m_new))``. A second pass forms
+    ``exp(x - m) / l``.
 
     Returns a dict: ``p`` (probabilities, same shape as x), ``m``, ``l``,
     ``lse`` (= m + ln l), ``trace`` (per block: m, correction, l for the
@@ -245,83 +257,89 @@ def online_softmax(x, block_size: int):
     counting the first block).
     """
     x = np.asarray(x, dtype=np.float64)
+    width = x.shape[-1]
     lead = x.shape[:-1]
-    n = x.shape[-1]
-    m = np.full(lead + (1,), -np.inf)
-    l = np.zeros(lead + (1,))
-    rescales = np.zeros(lead, dtype=np.int64)
+    run_m = np.full(lead + (1,), -np.inf)
+    run_l = np.zeros(lead + (1,))
+    moved = np.zeros(lead, dtype=np.int64)
     trace = []
-    for start in range(0, n, block_size):
-        block = x[..., start:start + block_size]
-        m_new = np.maximum(m, block.max(axis=-1, keepdims=True))
-        with np.errstate(invalid="ignore"):
-            correction = np.exp(m - m_new)
-        correction = np.where(np.isneginf(m), 0.0, correction)
-        rescales += (m_new > m)[..., 0]
-        l = l * correction + np.exp(block - m_new).sum(axis=-1, keepdims=True)
-        m = m_new
-        first = (0,) * len(lead)
-        trace.append({"m": float(m[first + (0,)]), "correction": float(correction[first + (0,)]),
-                      "l": float(l[first + (0,)])})
-    p = np.exp(x - m) / l
-    return {"p": p, "m": m[..., 0], "l": l[..., 0], "lse": m[..., 0] + np.log(l[..., 0]),
-            "trace": trace, "rescales": rescales}
+    first_row = (0,) * len(lead) + (0,)
+    for part in np.split(x, np.arange(block_size, width, block_size), axis=-1):
+        part_m = part.max(axis=-1, keepdims=True)
+        part_l = np.exp(part - part_m).sum(axis=-1, keepdims=True)
+        new_m = np.maximum(run_m, part_m)
+        correction = _rebase(run_m, new_m)
+        moved += (new_m > run_m)[..., 0]
+        run_l = run_l * correction + part_l * np.exp(part_m - new_m)
+        run_m = new_m
+        trace.append({"m": float(run_m[first_row]), "correction": float(correction[first_row]),
+                      "l": float(run_l[first_row])})
+    p = np.exp(x - run_m) / run_l
+    return {"p": p, "m": run_m[..., 0], "l": run_l[..., 0], "lse": run_m[..., 0] + np.log(run_l[..., 0]),
+            "trace": trace, "rescales": moved}
+
+
+def _tile_edges(length: int, block: int):
+    """(start, stop) of the consecutive blocks of ``block`` rows covering ``length``."""
+    starts = np.arange(0, length, block)
+    return [(int(lo), int(min(lo + block, length))) for lo in starts]
 
 
 def tiled_attention(q, k, v, causal: bool, scale: float, block_q: int, block_k: int):
-    """The tiled two-level loop of [P3] section 4, in fp64, for one head.
+    """The tiled two-level computation of [P3] section 4, in fp64, for one head.
 
-    Outer loop over query blocks of ``block_q`` rows; inner loop over key/value
-    blocks of ``block_k`` rows. Per query row: running max ``m``, running sum
-    ``l`` and accumulator ``acc``; per tile
-    ``m_new = max(m, rowmax(s))``, ``c = exp(m - m_new)``, ``p = exp(s - m_new)``,
-    ``l = l c + rowsum(p)``, ``acc = acc c + p V_j``; after the inner loop
-    ``O = acc / l``. With ``causal``, a tile whose first key lies after the
-    block's last query is skipped ([P3] section 7) and diagonal tiles are
-    masked element-wise ([P3] section 5).
+    Query blocks of ``block_q`` rows each visit the key/value blocks of
+    ``block_k`` rows. Every (query block, key block) tile yields a partial
+    result relative to its own row maxima -- ``m_t = rowmax(s)``,
+    ``p = exp(s - m_t)``, ``l_t = rowsum(p)``, ``o_t = p V`` -- which is merged
+    into the query block's running ``(m, l, acc)`` by rebasing both sides to
+    ``m_new = max(m, m_t)``: ``acc = acc exp(m - m_new) + o_t exp(m_t - m_new)``
+    and likewise for ``l`` ([P3] section 3, "Partial softmaxes compose"; the
+    pages fold the two factors into one correction of the running state). After
+    the last tile ``O = acc / l``. With ``causal``, a tile whose first key lies
+    after the block's last query is skipped ([P3] section 7) and diagonal tiles
+    are masked element-wise ([P3] section 5).
 
     Returns ``(O, LSE, counters)``; counters follow [P3] section 8's tallies
-    (two matmuls of ``2 rows cols d`` FLOPs per computed tile; K and V tile
-    reads of ``rows`` ... ``cols d`` elements) plus tile and rescale counts.
+    (two matmuls, i.e. ``4 rows cols d`` FLOPs, and the K and V tiles read, per
+    computed tile) plus tile and rescale counts.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     n_q, d = q.shape
-    n_k = k.shape[0]
     O = np.empty((n_q, v.shape[1]))
     lse = np.empty(n_q)
     counters = {"tiles_computed": 0, "tiles_skipped": 0, "matmul_flops": 0,
                 "kv_elements_read": 0, "rescales": 0}
-    for i in range(0, n_q, block_q):
-        qi = q[i:i + block_q]
-        rows = qi.shape[0]
-        m = np.full((rows, 1), -np.inf)
-        l = np.zeros((rows, 1))
-        acc = np.zeros((rows, v.shape[1]))
-        for j in range(0, n_k, block_k):
-            if causal and j > i + rows - 1:
+    key_tiles = _tile_edges(k.shape[0], block_k)
+    for q_lo, q_hi in _tile_edges(n_q, block_q):
+        q_tile = q[q_lo:q_hi]
+        m = np.full((q_hi - q_lo, 1), -np.inf)
+        l = np.zeros((q_hi - q_lo, 1))
+        acc = np.zeros((q_hi - q_lo, v.shape[1]))
+        for k_lo, k_hi in key_tiles:
+            if causal and k_lo >= q_hi:  # every key of the tile is after every query
                 counters["tiles_skipped"] += 1
                 continue
-            kj, vj = k[j:j + block_k], v[j:j + block_k]
-            cols = kj.shape[0]
+            k_tile, v_tile = k[k_lo:k_hi], v[k_lo:k_hi]
             counters["tiles_computed"] += 1
-            counters["matmul_flops"] += 2 * (2 * rows * cols * d)
-            counters["kv_elements_read"] += 2 * cols * d
-            s = scale * (qi @ kj.T)
+            counters["matmul_flops"] += 4 * q_tile.shape[0] * k_tile.shape[0] * d
+            counters["kv_elements_read"] += k_tile.size + v_tile.size
+            s = (q_tile @ k_tile.T) * scale
             if causal:
-                s = np.where(_causal_mask(rows, cols, i, j), -np.inf, s)
-            m_new = np.maximum(m, s.max(axis=1, keepdims=True))
-            with np.errstate(invalid="ignore"):
-                c = np.exp(m - m_new)
-            c = np.where(np.isneginf(m), 0.0, c)
+                s = np.where(_causal_mask(q_hi - q_lo, k_hi - k_lo, q_lo, k_lo), -np.inf, s)
+            m_t = s.max(axis=1, keepdims=True)
+            p = np.exp(s - np.where(np.isneginf(m_t), 0.0, m_t))
+            m_new = np.maximum(m, m_t)
+            keep = _rebase(m, m_new)
+            take = _rebase(m_t, m_new)
             counters["rescales"] += int(np.sum((m_new > m) & ~np.isneginf(m)))
-            p = np.exp(s - m_new)
-            l = l * c + p.sum(axis=1, keepdims=True)
-            acc = acc * c + p @ vj
+            l = l * keep + p.sum(axis=1, keepdims=True) * take
+            acc = acc * keep + (p @ v_tile) * take
             m = m_new
-        O[i:i + rows] = acc / l
-        lse[i:i + rows] = m[:, 0] + np.log(l[:, 0])
+        O[q_lo:q_hi] = acc / l
+        lse[q_lo:q_hi] = m[:, 0] + np.log(l[:, 0])
     return O, lse, counters
 
 
@@ -332,27 +350,25 @@ def tiled_attention(q, k, v, causal: bool, scale: float, block_q: int, block_k: 
 
 def tile_schedule_counts(n: int, block_q: int, block_k: int, causal: bool,
                          batch: int = 1, heads: int = 1, dim: int = 64, elem: int = 4):
-    """Walk the tiled loop's schedule without arithmetic and tally it.
+    """The tiled schedule's tallies, without arithmetic ([P3] sections 7-8).
 
-    Counts per [P3] section 7 (skip rule ``j > i + rows - 1``) and section 8:
-    ``matmul_flops += 2 (2 b h rows cols d)`` and
-    ``hbm_bytes += 2 b h cols d elem`` per computed tile, plus one read of Q
-    and one write of O (``2 b h n d elem``) for the all-tensor traffic total.
+    A tile is computed unless causal masking hides it whole (its first key
+    after its last query). Per computed tile of ``rows`` queries and ``cols``
+    keys the two matmuls cost ``4 rows cols dim`` FLOPs per (batch, head), and
+    the K and V tiles are read from HBM (``2 cols dim`` elements); Q is read and
+    O written once (``2 n dim`` elements) for the all-tensor traffic total.
     """
-    computed = skipped = flops = kv_bytes = 0
-    for i in range(0, n, block_q):
-        rows = min(block_q, n - i)
-        for j in range(0, n, block_k):
-            cols = min(block_k, n - j)
-            if causal and j > i + rows - 1:
-                skipped += 1
-                continue
-            computed += 1
-            flops += 2 * (2 * batch * heads * rows * cols * dim)
-            kv_bytes += 2 * batch * heads * cols * dim * elem
-    qo_bytes = 2 * batch * heads * n * dim * elem
-    return {"computed": computed, "skipped": skipped, "matmul_flops": flops,
-            "hbm_bytes": kv_bytes + qo_bytes}
+    visible = [(q_hi - q_lo, k_hi - k_lo)
+               for q_lo, q_hi in _tile_edges(n, block_q)
+               for k_lo, k_hi in _tile_edges(n, block_k)
+               if not (causal and k_lo >= q_hi)]
+    total_tiles = len(_tile_edges(n, block_q)) * len(_tile_edges(n, block_k))
+    heads_total = batch * heads
+    pair_count = sum(rows * cols for rows, cols in visible)
+    key_rows = sum(cols for _, cols in visible)
+    return {"computed": len(visible), "skipped": total_tiles - len(visible),
+            "matmul_flops": 4 * heads_total * dim * pair_count,
+            "hbm_bytes": heads_total * dim * elem * (2 * key_rows + 2 * n)}
 
 
 def naive_counts(n: int, batch: int = 1, heads: int = 1, dim: int = 64, elem: int = 4):
