@@ -46,6 +46,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd.restype = _i
+        L.fa_bwd_noalloc.argtypes = [_vp] * 9 + [_i, _i, _i, _i, _i, _i, _f, _vp]
+        L.fa_bwd_noalloc.restype = _i
         L.fa_bwd_window.argtypes = [_vp] * 9 + [_vp, ctypes.c_size_t] + [_i, _i, _i, _i, _i, _i, _f, _vp]
         L.fa_bwd_window.restype = _i
         L.fa_bwd_prepare.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i, _i, _vp]
@@ -204,6 +206,26 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
                      B, Hq, Hkv, N, d, int(bool(causal)), sc, _stream_handle(stream, q.device))
     if r != FA_OK:
         raise FAError(r, "fa_bwd")
+    return dq, dk, dv
+
+
+def backward_noalloc(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+                     dq=None, dk=None, dv=None, stream=None):
+    """fa_bwd_noalloc: the backward without a caller workspace (the library's fixed scratch
+    array; calls that overlap on one device race on it)."""
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("do", do)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must match q")
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    sc = 0.0 if scale is None else float(scale)
+    r = lib().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, N, d, int(bool(causal)), sc,
+                             _stream_handle(stream, q.device))
+    if r != FA_OK:
+        raise FAError(r, "fa_bwd_noalloc")
     return dq, dk, dv
 
 

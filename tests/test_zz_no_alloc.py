@@ -61,3 +61,16 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
     dummy = 0x1000  # never dereferenced: the size check comes first and nothing is launched
     r = fn(*([dummy] * 9), 1, 32, 8, 8192, 128, 1, 0.0, None)
     assert r == -6, fa.strerror(r)
+
+
+def test_python_binding_matches_fa_bwd():
+    # fa.backward_noalloc marshals the same call: dK and dV (no reductions across CTAs) are
+    # bit-identical to fa_bwd's, dQ agrees to its fp32 reduction order.
+    fa, _ = _noalloc()
+    q, k, v, do = (t.cuda() for t in make_qkv(2, 4, 2, 257, 128, seed=43, with_do=True))
+    o, lse = fa.forward(q, k, v, True)
+    ref = fa.backward(q, k, v, o, do, lse, True)
+    got = fa.backward_noalloc(q, k, v, o, do, lse, True)
+    fa.check()
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    assert rel_fro(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy()) <= 1e-3
