@@ -14,9 +14,10 @@ runs the same per-GPU workload on its own GPU with no data-path collective (weak
 the timing uses a barrier and the max over ranks. `--impl reference` times the fp64 CPU
 oracle on the host cores on bounded samples of the same workload.
 `--batch B` shrinks the batch for profiling runs only; such a line is not a bench value.
-`--workload softmax_rows|splitkv|window|naive|sweep` times one of the extra workloads instead
-(the row softmax, split-KV, sliding window, S/P-through-HBM attention, and a sequence-length
-sweep at B*N = 16384) and prints its own JSON line.
+`--workload softmax_rows|splitkv|window|naive|sweep|long` times one of the extra workloads
+instead (the row softmax, split-KV, sliding window, S/P-through-HBM attention, a
+sequence-length sweep at B*N = 16384, and the N = 131072 long-context forward) and prints its
+own JSON line.
 """
 
 from __future__ import annotations
@@ -623,6 +624,50 @@ def run_naive(args):
         "rows": rows}), flush=True)
 
 
+def run_long(args):
+    """Long context: B=1, Hq=32, Hkv=8, N=131072, d=128, causal, N(0,1)*0.5 from seed 4 (the
+    forward streams K and V with no extra device memory). Forward TFLOP/s, the tiles it computed
+    and skipped (fa_fwd_stats), the device memory the forward call allocated (none), and the
+    backward for reference."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    B, Hq, Hkv, N, d = 1, 32, 8, 131072, 128
+    q, k, v, do = (t.cuda() for t in make_qkv(B, Hq, Hkv, N, d, seed=4, value_scale=0.5, with_do=True))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, N, device=q.device)
+    fl = fwd_flops(B, Hq, N, d, True)
+    steps, warmup = max(1, min(args.steps, 5)), args.warmup
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    before = torch.cuda.max_memory_allocated()
+    t_fwd = _time_ms(lambda: fa.forward(q, k, v, True, out=o, lse=lse), steps, warmup)
+    extra = torch.cuda.max_memory_allocated() - before
+    counters = torch.zeros(3, dtype=torch.int64, device=q.device)
+    fa.forward(q, k, v, True, out=o, lse=lse, counters=counters)
+    done, skipped, raised = (int(x) for x in counters.tolist())
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=q.device)
+    t_bwd = _time_ms(lambda: fa.backward(q, k, v, o, do, lse, True, dq=dq, dk=dk, dv=dv, workspace=ws), steps, 1)
+    fa.check()
+    burst, _, _ = load_peaks()
+    T = N // 128
+    print(json.dumps({
+        "metric": "long-context forward TFLOP/s (bf16, B=1 Hq=32 Hkv=8 N=131072 d=128 causal)",
+        "value": round(fl / (t_fwd * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(t_fwd, 3), "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": "fa_fwd at N=131072 (and fa_bwd for reference)"},
+        "pct_of_peak_burst": round(100 * fl / (t_fwd * 1e-3) / 1e12 / burst, 2),
+        "tiles": {"computed": done, "skipped": skipped, "expected_computed": B * Hq * T * (T + 1) // 2,
+                  "skipped_fraction": round(skipped / (done + skipped), 6), "rows_rescaled": raised},
+        "forward_extra_device_bytes": int(extra),
+        "backward": {"tflops": round(BWD_FACTOR * fl / (t_bwd * 1e-3) / 1e12, 2), "ms": round(t_bwd, 3),
+                     "workspace_bytes": ws.numel()},
+        "gpu_launches": (steps + warmup + 1) + 3 * (steps + 1)}), flush=True)
+
+
 def _median_ms_cold(fn, steps, warmup, flush):
     """Median over `steps` single calls of `fn`, each timed alone with CUDA events after a write
     of `flush` (larger than L2), so that every call starts with its inputs in HBM only."""
@@ -716,7 +761,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
-    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep"],
+    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep", "long"],
                     default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
     ap.add_argument("--small-configs-child", action="store_true", help=argparse.SUPPRESS)
@@ -736,6 +781,8 @@ def main():
         run_naive(args)
     elif args.workload == "sweep":
         run_sweep(args)
+    elif args.workload == "long":
+        run_long(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
