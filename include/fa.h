@@ -132,7 +132,9 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
  *     dV = P^T dO,  dP = dO V^T,  delta = rowsum(dO * O),  dS = P * (dP - delta),
  *     dQ = scale dS K,  dK = scale dS^T Q.
  * workspace: device buffer of at least fa_bwd_workspace_bytes() bytes, 16-byte aligned;
- * its contents on entry do not matter. dq is not deterministic bit for bit (fp32 atomics).
+ * its contents on entry do not matter. dq is not deterministic bit for bit: the fp32 dQ
+ * contributions of different key tiles are added by bulk tensor reductions in whichever order
+ * the CTAs reach them.
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
            const float *lse, void *dq, void *dk, void *dv,
@@ -185,7 +187,8 @@ int fa_bwd_finalize(void *dq, void *workspace, size_t workspace_bytes,
  *   - Returns FA_ERR_WORKSPACE, launching nothing, when fa_bwd_workspace_bytes(B, Hq, Hkv, N, d)
  *     exceeds FA_BWD_NOALLOC_MAX_BYTES (64 MiB: e.g. B*Hq*N up to about 129,000 query rows
  *     at d = 128, or 254,000 at d = 64; rows are counted after rounding N up to a multiple of 128).
- *   - The first call on a device looks up the array's device address (with that device
+ *   - The first call on a device (and the first after the device context is re-created, e.g.
+ *     by cudaDeviceReset) looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - All calls on a device share the one array. Calls whose kernels overlap on the GPU (on
  *     different streams, or from different threads) race on it and give wrong results;

@@ -42,7 +42,8 @@ struct DeviceState {
   bool init = false;
   bool supported = false;
   int num_sms = 0;
-  uint32_t* status = nullptr;  // device address of g_fa_status on this device
+  uint32_t* status = nullptr;  // device address of g_fa_status in the context below
+  unsigned long long ctx = 0;  // id of the context `status` was looked up in (0: none yet)
 };
 DeviceState g_devices[kMaxDevices];
 std::mutex g_mutex;
@@ -50,8 +51,13 @@ std::mutex g_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// Looks up (once per device, with that device current) whether it is an sm_103 part and the
-// device address of its status word.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Looks up whether the current device is an sm_103 part (once per device) and the device
+// address of its status word (again whenever the current context is not the one the address
+// was taken in: a context re-created after cudaDeviceReset loads the module afresh).
 int current_device(uint32_t** status, int* num_sms = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
@@ -65,18 +71,47 @@ int current_device(uint32_t** status, int* num_sms = nullptr) {
       return FA_ERR_LAUNCH;
     s.supported = (major == 10 && minor == 3);
     if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_LAUNCH;
-    if (s.supported) {
-      void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
-      s.status = static_cast<uint32_t*>(addr);
-    }
     s.init = true;
   }
   if (!s.supported) return FA_ERR_DEVICE;
-  if (status) *status = s.status;
+  if (status) {
+    const unsigned long long ctx = fa::current_context_id();
+    if (s.status == nullptr || ctx == 0 || ctx != s.ctx) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
+      s.status = static_cast<uint32_t*>(addr);
+      s.ctx = fa::current_context_id();  // the lookup made the primary context current if it was not
+    }
+    *status = s.status;
+  }
   if (num_sms) *num_sms = s.num_sms;
   return FA_OK;
 }
+
+}  // namespace
+
+unsigned long long fa::current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  });
+  if (g_ctx_current == nullptr || g_ctx_get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return g_ctx_get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+int fa::check_current_device() { return current_device(nullptr); }
+
+namespace {
 
 bool load_encoder() {
   std::call_once(g_encode_once, [] {
@@ -249,6 +284,17 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   return fa::launch_fwd(a) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
+
+}  // namespace
+
+int fa::check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dout, const void* lse,
+                       const void* dq, const void* dk, const void* dv, int B, int Hq, int Hkv, int N, int d) {
+  FA_TRY(check_sizes(B, Hq, Hkv, N, d));
+  for (const void* p : {q, k, v, o, dout, lse, dq, dk, dv}) FA_TRY(check_ptr(p));
+  return FA_OK;
+}
+
+namespace {
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
              void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int N,

@@ -76,4 +76,17 @@ int launch_naive_fwd(const void* q, const void* k, const void* v, void* o, float
 
 inline int round_up_tile(int n) { return (n + kTile - 1) / kTile * kTile; }
 
+// Unique id of the calling thread's current CUDA context, 0 if there is none (or it cannot be
+// read). Context ids are never reused, so a context re-created after cudaDeviceReset has a new
+// one: device addresses of module variables cached under an id stay valid while it matches.
+unsigned long long current_context_id();
+
+// FA_OK if the current device is an sm_103 GPU; FA_ERR_DEVICE (or FA_ERR_LAUNCH) otherwise.
+int check_current_device();
+
+// The argument checks of fa_bwd that need no CUDA call (sizes, pointers): FA_OK or the status
+// fa_bwd would return for them.
+int check_bwd_args(const void* q, const void* k, const void* v, const void* o, const void* dout, const void* lse,
+                   const void* dq, const void* dk, const void* dv, int B, int Hq, int Hkv, int N, int d);
+
 }  // namespace fa

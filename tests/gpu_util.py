@@ -8,7 +8,13 @@ specification of this library and written here once:
             oracle by up to half a bf16 ulp (0.0156 for |O| in [4, 8)). The 1e-2 bound is
             therefore applied to the distance between O_ref and the interval of reals that
             round to the stored bf16 value: |O - O_ref| - ulp_bf16(O)/2 <= 1e-2.
-  backward: ||X - X_ref||_F / ||X_ref||_F <= 2e-2 for X in dQ, dK, dV
+  backward: ||X - X_ref||_F / ||X_ref||_F <= 2e-2 for X in dQ, dK, dV, and element by element
+            max |X - X_ref| / max |X_ref| <= 2e-2 as well, so that one wrong row or column
+            (a few elements out of millions, invisible in the Frobenius ratio) still fails.
+            Where the kernel's arithmetic stands: P and dS are rounded to bf16 before their
+            products (relative error 2^-9 per term, summed with random signs) and the result is
+            stored in bf16 (2^-9 of the element at most), so both ratios come out near 1e-3 to
+            5e-3; 2e-2 leaves a margin of about four.
 The reference is always the fp64 CPU oracle on the same bf16 inputs.
 """
 
@@ -21,6 +27,7 @@ from online_softmax_09_gb300.inputs import to_f64
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_REL_TOL = 2e-2
+GRAD_MAX_TOL = 2e-2
 
 
 def fa_mod():
@@ -93,3 +100,25 @@ def rel_fro(x, ref, floor=0.0):
     vanishes (e.g. N = 1, where the single weight is 1 and dQ = dK = 0 exactly)."""
     x = np.asarray(x, dtype=np.float64)
     return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), floor, 1e-300))
+
+
+def max_rel(x, ref, floor=0.0):
+    """max |x - ref| / max(max |ref|, floor): the largest element-wise error against the
+    tensor's scale (the floor as in rel_fro)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if not ref.size:
+        return 0.0
+    return float(np.max(np.abs(x - ref)) / max(float(np.max(np.abs(ref))), floor, 1e-300))
+
+
+def assert_grad_close(name, x, ref, fro_floor=0.0, max_floor=0.0, what=""):
+    """Both gradient bounds (relative Frobenius and element-wise max, each with its floor as in
+    rel_fro); returns the two ratios."""
+    x = np.asarray(x, dtype=np.float64)
+    assert np.all(np.isfinite(x)), f"{what} {name}: non-finite values"
+    fro, mx = rel_fro(x, ref, fro_floor), max_rel(x, ref, max_floor)
+    msg = f"{what} {name}: relative Frobenius {fro:.3e}, element-wise max |d| / max |ref| {mx:.3e}"
+    print(msg)
+    assert fro <= GRAD_REL_TOL and mx <= GRAD_MAX_TOL, msg
+    return fro, mx

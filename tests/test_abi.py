@@ -123,3 +123,18 @@ def test_splitkv_auto_choice(L):
     assert L.fa_fwd_splitkv_auto(1, 3, 2, 300, 128, 1, 152) < 0      # Hq % Hkv != 0
     assert L.fa_fwd_splitkv_auto(1, 2, 1, 300, 96, 1, 152) < 0       # d = 96
     assert L.fa_fwd_splitkv_auto(1, 2, 1, 300, 128, 1, 0) < 0        # no SMs
+
+
+def test_noalloc_checks_arguments_before_any_cuda_call(L):
+    # fa_bwd_noalloc takes its checks in the order of the other entry points: sizes and
+    # pointers, then its fixed scratch's size limit, both before any CUDA call (so they hold on
+    # a machine without a GPU), then the device, then the scratch lookup.
+    fn = L.fa_bwd_noalloc
+    fn.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    ok = [0x1000] * 9
+    assert fn(None, *ok[1:], 1, 1, 1, 128, 128, 1, 0.0, None) == -1      # null pointer
+    assert fn(*ok[:8], 0x1008, 1, 1, 1, 128, 128, 1, 0.0, None) == -3    # misaligned dv
+    assert fn(*ok, 1, 3, 2, 128, 128, 1, 0.0, None) == -1                # Hq % Hkv != 0
+    assert fn(*ok, 1, 1, 1, 128, 96, 1, 0.0, None) == -2                 # unsupported d
+    assert fn(*ok, 1, 32, 8, 8192, 128, 1, 0.0, None) == -6              # beyond the 64 MiB scratch

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import GRAD_REL_TOL, fa_mod, rel_fro, sample_rows
+from gpu_util import assert_grad_close, fa_mod, rel_fro, sample_rows
 from online_softmax_09_gb300.inputs import make_qkv, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -25,14 +25,13 @@ def gpu_fwd_bwd(q, k, v, do, causal, scale=None):
 def check_full(q, k, v, do, causal, scale):
     _, _, dq, dk, dv = gpu_fwd_bwd(q, k, v, do, causal, scale)
     ref = oracle.attention_backward(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal, scale)
+    # dV never vanishes; it sets the gradient scale where the exact dQ and dK do (N = 1).
+    fro_floor = 1e-3 * np.linalg.norm(ref[2])
+    max_floor = 1e-3 * float(np.max(np.abs(ref[2])))
     errs = []
-    floor = 1e-3 * np.linalg.norm(ref[2])  # dV never vanishes; it sets the gradient scale
     for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        g = g.float().cpu().numpy()
-        assert np.all(np.isfinite(g)), name
-        e = rel_fro(g, r, floor)
-        errs.append(e)
-        assert e <= GRAD_REL_TOL, f"{name}: relative Frobenius error {e:.3e} > {GRAD_REL_TOL}"
+        fro, _ = assert_grad_close(name, g.float().cpu().numpy(), r, fro_floor, max_floor, what="full")
+        errs.append(fro)
     return errs
 
 
@@ -59,18 +58,22 @@ def test_ragged_and_gqa_shapes(N, d, heads, causal):
 
 
 def test_llama8b_shape_b4_h32_kv8_n4096_d128_causal():
-    # GQA 4:1, N(0,1)*0.5 from seed 2; full backward checked for kv groups (0,0) and (0,7).
+    # GQA 4:1, N(0,1)*0.5 from seed 2; the full backward of kv groups (0,0) and (0,7), in the
+    # first of the kernel's two launch bands of 16 (batch, kv head) pairs, and (3,7), the last
+    # group of the second band.
     q, k, v, do = make_qkv(4, 32, 8, 4096, 128, seed=2, value_scale=0.5, with_do=True)
     scale = 1 / math.sqrt(128)
     _, _, dq, dk, dv = gpu_fwd_bwd(q, k, v, do, True)
-    groups = [(0, 0), (0, 7)]
-    ref = oracle.attention_backward(to_f64(q[:1]), to_f64(k[:1]), to_f64(v[:1]), to_f64(do[:1]), True, scale,
-                                    heads=groups)
-    for b, hk in groups:
-        hq = slice(4 * hk, 4 * hk + 4)
-        assert rel_fro(dq[b, hq].float().cpu().numpy(), ref[0][b, hq]) <= GRAD_REL_TOL
-        assert rel_fro(dk[b, hk].float().cpu().numpy(), ref[1][b, hk]) <= GRAD_REL_TOL
-        assert rel_fro(dv[b, hk].float().cpu().numpy(), ref[2][b, hk]) <= GRAD_REL_TOL
+    for b, groups in ((0, [(0, 0), (0, 7)]), (3, [(0, 7)])):
+        bs = slice(b, b + 1)
+        ref = oracle.attention_backward(to_f64(q[bs]), to_f64(k[bs]), to_f64(v[bs]), to_f64(do[bs]), True, scale,
+                                        heads=groups)
+        for _, hk in groups:
+            hq = slice(4 * hk, 4 * hk + 4)
+            what = f"(b={b}, kv head {hk})"
+            assert_grad_close("dq", dq[b, hq].float().cpu().numpy(), ref[0][0, hq], what=what)
+            assert_grad_close("dk", dk[b, hk].float().cpu().numpy(), ref[1][0, hk], what=what)
+            assert_grad_close("dv", dv[b, hk].float().cpu().numpy(), ref[2][0, hk], what=what)
 
 
 @pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
@@ -94,8 +97,7 @@ def test_sequence_sweep_16k_tokens(N, d):
             idx = torch.as_tensor(rows, device=dq.device)
             gq, gk, gv = dq[b, h, idx], dk[b, h, idx], dv[b, h, idx]
         for name, g, r in (("dq", gq, rq), ("dk", gk, rk), ("dv", gv, rv)):
-            e = rel_fro(g.float().cpu().numpy(), r)
-            assert e <= GRAD_REL_TOL, f"causal={causal} {name}: {e:.3e}"
+            assert_grad_close(name, g.float().cpu().numpy(), r, what=f"causal={causal}")
 
 
 def test_dk_dv_deterministic_and_workspace_reuse():

@@ -4,18 +4,20 @@ Such callers (a plugin whose host runtime owns all device memory, a loop where c
 implicit synchronisation is not allowed) get the workspace from a fixed array inside the
 library instead of passing one. These tests call the entry point through the C ABI and check
 it against fa_bwd, the entry point that takes a caller-allocated workspace, on two calls in a
-row with different shapes, so a second call cannot pass on stale scratch contents. The file
-is named so that pytest collects it last.
+row with different shapes, so a second call cannot pass on stale scratch contents, and one
+call directly against the fp64 oracle. The file is named so that pytest collects it last.
 """
 
 import ctypes
+import math
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_util import GRAD_REL_TOL, fa_mod, rel_fro
-from online_softmax_09_gb300.inputs import make_qkv
+import oracle
+from gpu_util import GRAD_REL_TOL, assert_grad_close, fa_mod, rel_fro
+from online_softmax_09_gb300.inputs import make_qkv, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +54,25 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row():
     fa, fn = _noalloc()
     _compare_once(fa, fn, 2, 4, 2, 640, 128, True, seed=41)
     _compare_once(fa, fn, 1, 6, 3, 300, 64, False, seed=42)
+
+
+def test_noalloc_matches_the_oracle():
+    # One call checked against the fp64 oracle itself, with the same bounds as every backward
+    # parity test (relative Frobenius and element-wise), on a grouped, ragged causal shape.
+    fa, fn = _noalloc()
+    B, Hq, Hkv, N, d = 2, 4, 2, 333, 128
+    qh, kh, vh, doh = make_qkv(B, Hq, Hkv, N, d, seed=44, with_do=True)
+    q, k, v, do = (t.cuda() for t in (qh, kh, vh, doh))
+    o, lse = fa.forward(q, k, v, True)
+    got = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+    stream = torch.cuda.current_stream().cuda_stream
+    r = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+           got[0].data_ptr(), got[1].data_ptr(), got[2].data_ptr(), B, Hq, Hkv, N, d, 1, 0.0, stream)
+    assert r == 0, fa.strerror(r)
+    fa.check()
+    ref = oracle.attention_backward(to_f64(qh), to_f64(kh), to_f64(vh), to_f64(doh), True, 1 / math.sqrt(d))
+    for name, g, w in zip(("dq", "dk", "dv"), got, ref):
+        assert_grad_close(name, g.float().cpu().numpy(), w, what="fa_bwd_noalloc")
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
