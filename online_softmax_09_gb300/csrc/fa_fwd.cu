@@ -31,7 +31,7 @@
 // a row dominated by one key that mismatch would show in O at bf16's relative precision. So each
 // tile's largest weight is recomputed exactly as pass 2 computes it, its bf16 rounding error is
 // accumulated in e (rescaled like l), and O is divided by l + e; LSE keeps the fp32 l.
-// S is read from TMEM twice (once for the row max, once for P) to keep registers low.
+// Each row's S is read from TMEM once into registers (128 values per thread).
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -284,98 +284,117 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      uint32_t gk = 0, gv = 0;  // K and V tiles consumed so far
-      uint32_t qn[2] = {0, 0};  // items in which query tile t was active
-      uint32_t pc[2] = {0, 0};  // P.V MMAs issued for tile t
-      // S_t = Q_t K^T with K tile number g; `ready`: K tile g's full barrier was already waited
-      // on for the other query tile.
-      auto issue_s = [&](int t, uint32_t g, bool ready) -> bool {
-        const uint32_t sk = g % NK;
-        if (!ready && !mbar_wait(bar(L::bKFull + sk), (g / NK) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t q_base = sQ + t * L::kTileBytes;
-        const uint32_t k_base = sK + sk * L::kTileBytes;
+    // The whole warp runs the issue loop, so its counters, barrier phases and descriptors are
+    // warp-uniform; one elected lane issues each group of MMAs and each commit. (A single-lane
+    // loop paced the tensor core: its issue of one MMA took ~85 cycles against the 64 the MMA
+    // runs, and each satisfied wait and the loop bookkeeping another ~100.)
+    constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
+    // Descriptor bases of the Q tiles and the K and V rings; a tile or an MMA step adds its byte
+    // offset / 16 to the start-address field (every shared address fits that 14-bit field).
+    const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dK = sdesc_sw128(sK, 16, 1024);
+    const uint64_t dV = sdesc_sw128(sV, 16384, 1024);
+    uint32_t gk = 0, gv = 0;  // K and V tiles consumed so far
+    uint32_t qn[2] = {0, 0};  // items in which query tile t was active
+    uint32_t pc[2] = {0, 0};  // P.V MMAs issued for tile t
+    auto commit = [&](uint32_t b) {
+      if (elect_one()) mma_commit(b);
+      __syncwarp();
+    };
+    // S_t = Q_t K^T with K tile number g; `ready`: K tile g's full barrier was already waited
+    // on for the other query tile.
+    auto issue_s = [&](int t, uint32_t g, bool ready) -> bool {
+      const uint32_t sk = g % NK;
+      if (!ready && !mbar_wait_warp(bar(L::bKFull + sk), (g / NK) & 1, ctl)) return false;
+      tc_fence_after();
+      const uint64_t a = dQ + (uint32_t)(t * (L::kTileBytes >> 4));
+      const uint64_t bk = dK + sk * (uint32_t)(L::kTileBytes >> 4);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major, 128B swizzle: 64-element column blocks 16 KB apart, 16 elements = 32 B.
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + 128 * t, sdesc_sw128(q_base + off, 16, 1024), sdesc_sw128(k_base + off, 16, 1024), idS,
-                 kk > 0);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + 128 * t, a + off, bk + off, idS, kk > 0);
         }
         mma_commit(bar(L::bSFull + t));
-        return true;
-      };
-      // O_t += P_t V with V tile number g. O_t's completion is signalled only after an item's last
-      // P.V (for the epilogue): each earlier one is followed by S_t's next score MMA, whose
-      // completion (which the softmax warps wait for) implies it.
-      auto issue_pv = [&](int t, uint32_t g, bool first, bool last, bool ready) -> bool {
-        const uint32_t sv = g % NV;
-        if (!mbar_wait(bar(L::bPFull + t), pc[t] & 1, ctl)) return false;
-        if (!ready && !mbar_wait(bar(L::bVFull + sv), (g / NV) & 1, ctl)) return false;
-        // The first P.V of an item overwrites O_t: the previous item's epilogue must be done.
-        if (first && qn[t] > 1 && !mbar_wait(bar(L::bOFree + t), (qn[t] - 2) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t v_base = sV + sv * L::kTileBytes;
+      }
+      __syncwarp();
+      return true;
+    };
+    // O_t += P_t V with V tile number g. O_t's completion is signalled only after an item's last
+    // P.V (for the epilogue): each earlier one is followed by S_t's next score MMA, whose
+    // completion (which the softmax warps wait for) implies it.
+    auto issue_pv = [&](int t, uint32_t g, bool first, bool last, bool ready) -> bool {
+      const uint32_t sv = g % NV;
+      if (!mbar_wait_warp(bar(L::bPFull + t), pc[t] & 1, ctl)) return false;
+      if (!ready && !mbar_wait_warp(bar(L::bVFull + sv), (g / NV) & 1, ctl)) return false;
+      // The first P.V of an item overwrites O_t: the previous item's epilogue must be done.
+      if (first && qn[t] > 1 && !mbar_wait_warp(bar(L::bOFree + t), (qn[t] - 2) & 1, ctl)) return false;
+      tc_fence_after();
+      const uint64_t bv = dV + sv * (uint32_t)(L::kTileBytes >> 4);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           // V as the MN-major B operand: 16 keys = 2 swizzle atoms of 8 rows x 128 B.
-          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, sdesc_sw128(v_base + kk * 2048, 16384, 1024),
-                 idO, (!first || kk > 0));
+          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, bv + (uint32_t)(kk * (2048 >> 4)), idO,
+                 (!first || kk > 0));
         }
         if (last) mma_commit(bar(L::bOFull + t));
-        ++pc[t];
-        return true;
-      };
-      bool ok = true;
-      for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
-        const int k = fwd_item_index(r, p.num_items);
-        if (k < 0) continue;
-        const FwdItem it = fwd_item<kWin, kSplit>(k, p);
-        if (it.n_max == 0) continue;
-        bool k_ready = false;
+      }
+      __syncwarp();
+      ++pc[t];
+      return true;
+    };
+    bool ok = true;
+    for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+      const int k = fwd_item_index(r, p.num_items);
+      if (k < 0) continue;
+      const FwdItem it = fwd_item<kWin, kSplit>(k, p);
+      if (it.n_max == 0) continue;
+      bool k_ready = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!ok) break;
+        if (it.b[t] == it.a[t]) continue;
+        if (!(ok = mbar_wait_warp(bar(L::bQ + t), qn[t] & 1, ctl))) break;
+        ++qn[t];
+        tc_fence_after();
+        if (it.a[t] == 0) {  // score MMA of the item's first key tile
+          if (!(ok = issue_s(t, gk, k_ready))) break;
+          k_ready = true;
+          if (it.b[t] == 1) commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
+        }
+      }
+      if (!ok) break;
+      commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
+      for (int j = 0; ok && j < it.n_max; ++j) {
+        bool v_ready = false, k_next_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (!ok) break;
-          if (it.b[t] == it.a[t]) continue;
-          if (!(ok = mbar_wait(bar(L::bQ + t), qn[t] & 1, ctl))) break;
-          ++qn[t];
-          tc_fence_after();
-          if (it.a[t] == 0) {  // score MMA of the item's first key tile
-            if (!(ok = issue_s(t, gk, k_ready))) break;
-            k_ready = true;
-            if (it.b[t] == 1) mma_commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
+          if (it.a[t] <= j && j < it.b[t]) {
+            if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
+            v_ready = true;
+          }
+          if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
+            if (!(ok = issue_s(t, gk + j + 1, k_next_ready))) break;
+            k_next_ready = true;
+            if (j + 2 == it.b[t]) commit(bar(L::bQEmpty + t));
           }
         }
         if (!ok) break;
-        mma_commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
-        for (int j = 0; ok && j < it.n_max; ++j) {
-          bool v_ready = false, k_next_ready = false;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (it.a[t] <= j && j < it.b[t]) {
-              if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
-              v_ready = true;
-            }
-            if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
-              if (!(ok = issue_s(t, gk + j + 1, k_next_ready))) break;
-              k_next_ready = true;
-              if (j + 2 == it.b[t]) mma_commit(bar(L::bQEmpty + t));
-            }
-          }
-          if (!ok) break;
-          mma_commit(bar(L::bVEmpty + (gv + j) % NV));
-          if (j + 1 < it.n_max) mma_commit(bar(L::bKEmpty + (gk + j + 1) % NK));
-        }
-        gk += it.n_max;
-        gv += it.n_max;
+        commit(bar(L::bVEmpty + (gv + j) % NV));
+        if (j + 1 < it.n_max) commit(bar(L::bKEmpty + (gk + j + 1) % NK));
       }
-      if (*abort_flag) {  // wait for issued MMAs before tensor memory is released
+      gk += it.n_max;
+      gv += it.n_max;
+    }
+    if (*abort_flag) {  // wait for issued MMAs before tensor memory is released
+      if (elect_one()) {
         mma_commit(bar(L::bDrain));
         drain_wait(bar(L::bDrain), 0);
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
@@ -418,21 +437,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                (kWin && kv0 < qt * kTile + kTile - p.window);
         const int lim = min(p.N - 1, p.causal ? row : p.N - 1) - kv0;
         const int lo = kWin ? row - p.window + 1 - kv0 : -kTile;
-        // Pass 1: row max.
-        float mx = -INFINITY;
+        // The row's 128 scores, read from TMEM once: four 32-column loads in flight together.
+        uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; c += 2) {
-          uint32_t a[32], b2[32];
-          tmem_ld32(tS + c * 32, a);
-          tmem_ld32(tS + (c + 1) * 32, b2);
-          tmem_ld_wait(a);
-          tmem_ld_wait(b2);
-          if (need_mask) {
-            mask32(a, c * 32, lo, lim);
-            mask32(b2, (c + 1) * 32, lo, lim);
-          }
-          mx = max64(a, b2, mx);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mask32(sr[c], c * 32, lo, lim);
         }
+        const float mx = max64(sr[2], sr[3], max64(sr[0], sr[1], -INFINITY));
         // Reference max in base-2 units, moved to the true max only when some row of the warp
         // has outgrown it by more than kRescaleLog2 (always on the first tile, where
         // m_run = -inf); correction exp(m_old - m_new) (0 on the first tile).
@@ -445,50 +460,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         m_run = m_new;
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         {
-          // This tile's largest weight, bit-identical to its value in pass 2 (same correctly
+          // This tile's largest weight, bit-identical to its value below (same correctly
           // rounded fma and exp2), and the error its bf16 rounding makes in the P.V MMA.
           const float pmx = ex2(fmaf(mx, sl2, -m_use));
           e_run = e_run * corr + (__uint_as_float(pack_bf16(pmx, 0.f) << 16) - pmx);
         }
-        if (j > 0) {
-          // O += P_{j-1} V was issued before S_j and has completed with it.
-          if (resc) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tO + c * 32, o);
-              tmem_ld_wait(o);
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
-                                      make_float2(corr, corr));
-                o[i] = __float_as_uint(r.x);
-                o[i + 1] = __float_as_uint(r.y);
-              }
-              tmem_st32(tO + c * 32, o);
-            }
-          }
-        }
-        // Pass 2: P = 2^(S*scale*log2e - m) as bf16 over the S columns already read, and row sum.
+        // P = 2^(S*scale*log2e - m) as bf16 over the S columns (all already in registers), and
+        // the row sum.
         float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tS + c * 32, a);
-          tmem_ld_wait(a);
-          if (need_mask) mask32(a, c * 32, lo, lim);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float2 x = fma2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), sl2x2, negm);
+            const float2 x = fma2(make_float2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2x2, negm);
             const float2 pp = make_float2(ex2(x.x), ex2(x.y));
             sum[(i >> 1) & 1] = add2(sum[(i >> 1) & 1], pp);
             pk[i >> 1] = pack_bf16(pp.x, pp.y);
           }
-          // P chunk c covers columns [16c, 16c+16): S columns that pass 2 has already read.
+          // P chunk c covers columns [16c, 16c+16).
           tmem_st16(tS + c * 16, pk);
+        }
+        // O += P_{j-1} V was issued before S_j and has completed with it; a rescale of O must
+        // land before this tile's P.V, which waits for the arrival below.
+        if (j > 0 && resc) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 r = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])),
+                                    make_float2(corr, corr));
+              o[i] = __float_as_uint(r.x);
+              o[i + 1] = __float_as_uint(r.y);
+            }
+            tmem_st32(tO + c * 32, o);
+          }
         }
         l_run = l_run * corr + ((sum[0].x + sum[1].x) + (sum[0].y + sum[1].y));
         tmem_st_wait();
