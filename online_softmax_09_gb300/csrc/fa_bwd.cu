@@ -314,82 +314,105 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dK += dS_i^T Q_i, then dP_{i+1}^T = V dO_{i+1}^T. dP does not depend on P, so it is issued
     // as soon as its TMEM columns are free (dQ_i drained), ahead of the P phase it will meet:
     // the softmax warps then go from P_{i+1} straight to dS_{i+1}. The dQ drain overlaps dK.
-    if (lane == 0) {
-      constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
-      constexpr uint32_t idDQ = idesc_bf16_f32(128, D, true, true);      // dQ
-      auto issue_s = [&](int it) {  // S^T = K_n Q_it^T into tS
-        const uint32_t sQ = stage(it & 1) + L::kStQ;
+    // The whole warp runs the loop (warp-uniform counters, phases and descriptors); one elected
+    // lane issues each group of MMAs and each commit.
+    constexpr uint32_t idSS = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+    constexpr uint32_t idTS = idesc_bf16_f32(128, D, false, true);     // dV, dK
+    constexpr uint32_t idDQ = idesc_bf16_f32(128, D, true, true);      // dQ
+    // Descriptor bases (K-major with 16-byte leading offset; MN-major with 16 KB); an operand
+    // or MMA step adds its byte offset / 16 to the start-address field.
+    const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dK_mn = sdesc_sw128(sK, 16384, 1024);
+    const uint64_t dSt_k = sdesc_sw128(stage(0), 16, 1024), dSt_mn = sdesc_sw128(stage(0), 16384, 1024);
+    const uint64_t dDS_k = sdesc_sw128(sDS(0), 16, 1024), dDS_mn = sdesc_sw128(sDS(0), 16384, 1024);
+    constexpr uint32_t kStage16 = L::kStageBytes >> 4;
+    auto kmajor = [](int kk) -> uint32_t { return (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+    auto issue_s = [&](int it) {  // S^T = K_n Q_it^T into tS
+      const uint64_t q = dSt_k + (uint32_t)((it & 1) * kStage16 + (L::kStQ >> 4));
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tS, dK_k + kmajor(kk), q + kmajor(kk), idSS, kk > 0);
         mma_commit(bar(L::bSFull));
-      };
-      // dP^T_it = V_n dO_it^T into tdP, once dO_it has landed and dQ_{it-1} has been drained
-      // out of these columns.
-      auto issue_dp = [&](int it) -> bool {
-        if (!mbar_wait(bar(L::bDOFull + (it & 1)), (it >> 1) & 1, ctl)) return false;
-        if (it > 0 && !mbar_wait(bar(L::bDQFree), (it - 1) & 1, ctl)) return false;
-        tc_fence_after();
-        const uint32_t sDO = stage(it & 1) + L::kStDO;
+      }
+      __syncwarp();
+    };
+    // dP^T_it = V_n dO_it^T into tdP, once dO_it has landed and dQ_{it-1} has been drained
+    // out of these columns.
+    auto issue_dp = [&](int it) -> bool {
+      if (!mbar_wait_warp(bar(L::bDOFull + (it & 1)), (it >> 1) & 1, ctl)) return false;
+      if (it > 0 && !mbar_wait_warp(bar(L::bDQFree), (it - 1) & 1, ctl)) return false;
+      tc_fence_after();
+      const uint64_t dO = dSt_k + (uint32_t)((it & 1) * kStage16 + (L::kStDO >> 4));
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tdP, dV_k + kmajor(kk), dO + kmajor(kk), idSS, kk > 0);
         mma_commit(bar(L::bDPFull));
-        return true;
-      };
-      bool ok = mbar_wait(bar(L::bKV), 0, ctl) && mbar_wait(bar(L::bQFull), 0, ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        ok = n_iter > 0 && issue_dp(0);
       }
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it & 1;
-        const uint32_t sQ = stage(s) + L::kStQ;
-        const uint32_t sDO = stage(s) + L::kStDO;
-        // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand; dO_i waited for dP_i)
-        if (!(ok = mbar_wait(bar(L::bPReady), it & 1, ctl))) break;
-        tc_fence_after();
+      __syncwarp();
+      return true;
+    };
+    bool ok = mbar_wait_warp(bar(L::bKV), 0, ctl) && mbar_wait_warp(bar(L::bQFull), 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      ok = n_iter > 0 && issue_dp(0);
+    }
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it & 1;
+      const uint32_t st16 = (uint32_t)s * kStage16;
+      // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand; dO_i waited for dP_i)
+      if (!(ok = mbar_wait_warp(bar(L::bPReady), it & 1, ctl))) break;
+      tc_fence_after();
+      {
+        const uint64_t dO = dSt_mn + st16 + (L::kStDO >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tdV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, 16384, 1024), idTS, (it > 0 || kk > 0));
-        mma_commit(bar(L::bDVDone));
-        // S^T of the next query tile (P_i^T in these columns was read by the dV MMA above).
-        if (it + 1 < n_iter) {
-          if (!(ok = mbar_wait(bar(L::bQFull + (s ^ 1)), ((it + 1) >> 1) & 1, ctl))) break;
-          tc_fence_after();
-          issue_s(it + 1);
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tdV, tS + packed_col(kk), dO + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
+          mma_commit(bar(L::bDVDone));
         }
-        // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns, first,
-        // so the drain starts as early as possible; then dK += dS^T Q_i with the same
-        // shared-memory dS as the K-major A operand.
-        if (!(ok = mbar_wait(bar(L::bSmemDS), it & 1, ctl))) break;
-        tc_fence_after();
-        const uint32_t sds = sDS(s);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tdP, sdesc_sw128(sds + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024), idDQ,
-                 kk > 0);
-        mma_commit(bar(L::bDQFull));
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdK, sdesc_sw128(sds + off, 16, 1024), sdesc_sw128(sQ + kk * 2048, 16384, 1024), idTS,
-                 (it > 0 || kk > 0));
-        }
-        mma_commit(bar(L::bStageEmpty + s));
-        if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
+        __syncwarp();
       }
-      if (ok) mma_commit(bar(L::bFinal));
-      if (*abort_flag) {
+      // S^T of the next query tile (P_i^T in these columns was read by the dV MMA above).
+      if (it + 1 < n_iter) {
+        if (!(ok = mbar_wait_warp(bar(L::bQFull + (s ^ 1)), ((it + 1) >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        issue_s(it + 1);
+      }
+      // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns, first,
+      // so the drain starts as early as possible; then dK += dS^T Q_i with the same
+      // shared-memory dS as the K-major A operand.
+      if (!(ok = mbar_wait_warp(bar(L::bSmemDS), it & 1, ctl))) break;
+      tc_fence_after();
+      {
+        const uint32_t ds16 = L::kAliasDS ? st16 + (L::kStDO >> 4) : 0u;
+        const uint64_t ds_mn = (L::kAliasDS ? dSt_mn : dDS_mn) + ds16;
+        const uint64_t ds_k = (L::kAliasDS ? dSt_k : dDS_k) + ds16;
+        const uint64_t q_mn = dSt_mn + st16 + (L::kStQ >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tdP, ds_mn + (uint32_t)(kk * (2048 >> 4)), dK_mn + (uint32_t)(kk * (2048 >> 4)), idDQ, kk > 0);
+          mma_commit(bar(L::bDQFull));
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tdK, ds_k + kmajor(kk), q_mn + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
+          mma_commit(bar(L::bStageEmpty + s));
+        }
+        __syncwarp();
+      }
+      if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
+    }
+    if (ok) {
+      if (elect_one()) mma_commit(bar(L::bFinal));
+      __syncwarp();
+    }
+    if (*abort_flag) {
+      if (elect_one()) {
         mma_commit(bar(L::bDrain));
         drain_wait(bar(L::bDrain), 0);
       }
+      __syncwarp();
     }
   } else if (warp < 4 || warp >= 10) {
     // ------------------------------------------------------------------ softmax / dS warps
