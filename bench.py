@@ -14,10 +14,12 @@ runs the same per-GPU workload on its own GPU with no data-path collective (weak
 the timing uses a barrier and the max over ranks. `--impl reference` times the fp64 CPU
 oracle on the host cores on bounded samples of the same workload.
 `--batch B` shrinks the batch for profiling runs only; such a line is not a bench value.
-`--workload softmax_rows|splitkv|window|naive|sweep|long` times one of the extra workloads
-instead (the row softmax, split-KV, sliding window, S/P-through-HBM attention, a
-sequence-length sweep at B*N = 16384, and the N = 131072 long-context forward) and prints its
-own JSON line.
+`--workload softmax_rows|splitkv|window|naive|sweep|long|shape` times one of the extra
+workloads instead (the row softmax, split-KV, sliding window, S/P-through-HBM attention, a
+sequence-length sweep at B*N = 16384, the N = 131072 long-context forward, or the single shape
+given by --shape B,Hq,Hkv,N,d,causal) and prints its own JSON line. The default line also
+carries `targets`: the causal d=128 bar at N >= 4096 (forward >= 60 %, backward >= 45 % of the
+bf16 peak) on the sweep's shapes and the long-context forward.
 """
 
 from __future__ import annotations
@@ -850,6 +852,52 @@ def run_sweep(args):
         "gpu_launches": len(rows) * (args.warmup + args.steps) * 8, "rows": rows}), flush=True)
 
 
+def run_shape(args):
+    """One shape, timed: forward, whole backward (prepare, compute, finalize) and the backward
+    compute kernel alone, each the median of single calls with L2 flushed before each, with
+    TFLOP/s (algorithmic) and compulsory-byte GB/s. For profiling and for checking one point of the
+    sweep; not the headline metric."""
+    import torch
+
+    from online_softmax_09_gb300 import fa
+    from online_softmax_09_gb300.inputs import make_qkv
+
+    B, Hq, Hkv, N, d, causal = (int(x) for x in args.shape.split(","))
+    causal = bool(causal)
+    q, k, v, do = (t.cuda() for t in make_qkv(B, Hq, Hkv, N, d, seed=3, with_do=True))
+    o, lse = torch.empty_like(q), torch.empty(B, Hq, N, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device=q.device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fl = fwd_flops(B, Hq, N, d, causal)
+    t_f = _median_ms_cold(lambda: fa.forward(q, k, v, causal, out=o, lse=lse), args.steps, args.warmup, flush)
+    t_b = _median_ms_cold(lambda: fa.backward(q, k, v, o, do, lse, causal, dq=dq, dk=dk, dv=dv, workspace=ws),
+                          args.steps, args.warmup, flush)
+    fa.backward_stages(q, k, v, o, do, lse, dq, dk, dv, ws, causal)
+    t_c = _median_ms_cold(lambda: fa.backward_stages(q, k, v, o, do, lse, dq, dk, dv, ws, causal, only=(1,)),
+                          args.steps, args.warmup, flush)
+    fa.check()
+    burst, _, src = load_peaks()
+    qb, kvb = B * Hq * N * d * 2, B * Hkv * N * d * 2
+    fwd_bytes = 2 * qb + 2 * kvb + B * Hq * N * 4
+    bwd_bytes = 3 * qb + 4 * kvb + qb + B * Hq * N * 4
+    print(json.dumps({
+        "metric": f"attention TFLOP/s on one shape (bf16, B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal={causal})",
+        "value": round(fl / (t_f * 1e-3) / 1e12, 2), "unit": "TFLOP/s (forward)", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"fa_fwd / fa_bwd, B={B} Hq={Hq} Hkv={Hkv} N={N} d={d} causal={causal}, seed 3",
+                   "l2": "flushed before each call", "timing": "median of single calls"},
+        "fwd": {"ms": round(t_f, 4), "tflops": round(fl / (t_f * 1e-3) / 1e12, 1),
+                "pct_of_peak_burst": round(100 * fl / (t_f * 1e-3) / 1e12 / burst, 2),
+                "compulsory_gbs": round(fwd_bytes / (t_f * 1e-3) / 1e9, 1)},
+        "bwd": {"ms": round(t_b, 4), "tflops": round(BWD_FACTOR * fl / (t_b * 1e-3) / 1e12, 1),
+                "pct_of_peak_burst": round(100 * BWD_FACTOR * fl / (t_b * 1e-3) / 1e12 / burst, 2),
+                "compulsory_gbs": round(bwd_bytes / (t_b * 1e-3) / 1e9, 1)},
+        "bwd_compute": {"ms": round(t_c, 4), "tflops": round(BWD_FACTOR * fl / (t_c * 1e-3) / 1e12, 1)},
+        "peak": {"bf16_tflops_burst": burst, "source": src},
+        "gpu_launches": (args.steps + args.warmup) * 5 + 3}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -861,9 +909,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-targets", action="store_true", help="skip the N >= 4096 target shapes")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: override the batch size")
-    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep", "long"],
+    ap.add_argument("--workload", choices=["attention", "softmax_rows", "splitkv", "window", "naive", "sweep", "long",
+                                           "shape"],
                     default="attention",
                     help="attention (the headline metric) or one of the extra workloads")
+    ap.add_argument("--shape", default="32,16,16,512,128,1", help="B,Hq,Hkv,N,d,causal for --workload shape")
     ap.add_argument("--small-configs-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.small_configs_child:
@@ -883,6 +933,8 @@ def main():
         run_sweep(args)
     elif args.workload == "long":
         run_long(args)
+    elif args.workload == "shape":
+        run_shape(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -249,9 +249,11 @@ def backward_window(q, k, v, o, do, lse, window: int, scale: float | None = None
 
 
 def backward_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, causal: bool = False,
-                    scale: float | None = None, stream=None, between=None):
+                    scale: float | None = None, stream=None, between=None, only=None):
     """Run fa_bwd_prepare, fa_bwd_compute and fa_bwd_finalize; ``between(i)`` (optional)
-    is called before stage i (0, 1, 2) and after the last (3), e.g. to record CUDA events."""
+    is called before stage i (0, 1, 2) and after the last (3), e.g. to record CUDA events.
+    ``only`` (optional): the stage indices to run, e.g. ``(1,)`` for the compute stage alone on a
+    workspace an earlier prepare filled."""
     B, Hq, Hkv, N, d = _check_qkv(q, k, v)
     sc = 0.0 if scale is None else float(scale)
     h = _stream_handle(stream, q.device)
@@ -265,6 +267,8 @@ def backward_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, causal: bool = F
         lambda: L.fa_bwd_finalize(dq.data_ptr(), workspace.data_ptr(), nb, B, Hq, Hkv, N, d, sc, h),
     )
     for i, call in enumerate(calls):
+        if only is not None and i not in only:
+            continue
         if between is not None:
             between(i)
         r = call()
