@@ -21,6 +21,11 @@
 // the diagonal tile and a ragged last tile are masked element-wise.
 //
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// Separate-P mode (D = 64, where each O region leaves 64 columns free): P_t lives in
+// [320,384) / [448,512) instead of over S_t. The next score MMA of a tile then needs only that
+// its softmax warps have read S_t into registers (bSFree), not that P.V has consumed P, so it
+// leaves the tile's critical loop, which becomes the softmax alone; bPFree (a commit after each
+// P.V) tells the softmax warps when P_t may be rewritten and O_t rescaled.
 // The running max is kept in base-2 units (scores scaled by scale*log2 e) so P uses the
 // hardware exp2. P is taken against a reference max m_ref that follows the true running max
 // lazily: a warp rescales l and O (and moves m_ref of its rows to their true max) only when one
@@ -145,7 +150,9 @@ struct FwdSmem {
   static constexpr int bOFull = bPFull + 2;   // 2
   static constexpr int bQEmpty = bOFull + 2;  // 2: Q buffer t no longer read by MMAs
   static constexpr int bOFree = bQEmpty + 2;  // 2: O_t read out by the epilogue
-  static constexpr int bDrain = bOFree + 2;
+  static constexpr int bSFree = bOFree + 2;   // 2: S_t read into registers (separate-P mode)
+  static constexpr int bPFree = bSFree + 2;   // 2: P_t consumed by its P.V (separate-P mode)
+  static constexpr int bDrain = bPFree + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -185,6 +192,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = FwdSmem<D, NK, NV>;
+  // Separate-P mode (see the TMEM plan above) and the first TMEM column of P_0.
+  constexpr bool kSepP = (D == 64);
+  constexpr uint32_t kPCol = kSepP ? 256 + 64 : 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -208,6 +218,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar(L::bOFull + t), 1);
       mbar_init(bar(L::bQEmpty + t), 1);
       mbar_init(bar(L::bOFree + t), 128);
+      mbar_init(bar(L::bSFree + t), 128);
+      mbar_init(bar(L::bPFree + t), 1);
     }
     for (int s = 0; s < NK; ++s) {
       mbar_init(bar(L::bKFull + s), 1);
@@ -337,7 +349,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           // V as the MN-major B operand: 16 keys = 2 swizzle atoms of 8 rows x 128 B.
-          mma_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, bv + (uint32_t)(kk * (2048 >> 4)), idO,
+          mma_ts(tmem + 256 + 128 * t, tmem + kPCol + 128 * t + kk * 8, bv + (uint32_t)(kk * (2048 >> 4)), idO,
                  (!first || kk > 0));
         }
         if (last) mma_commit(bar(L::bOFull + t));
@@ -347,47 +359,106 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       return true;
     };
     bool ok = true;
-    for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
-      const int k = fwd_item_index(r, p.num_items);
-      if (k < 0) continue;
-      const FwdItem it = fwd_item<kWin, kSplit>(k, p);
-      if (it.n_max == 0) continue;
-      bool k_ready = false;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (!ok) break;
-        if (it.b[t] == it.a[t]) continue;
-        if (!(ok = mbar_wait_warp(bar(L::bQ + t), qn[t] & 1, ctl))) break;
-        ++qn[t];
-        tc_fence_after();
-        if (it.a[t] == 0) {  // score MMA of the item's first key tile
-          if (!(ok = issue_s(t, gk, k_ready))) break;
-          k_ready = true;
-          if (it.b[t] == 1) commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
-        }
-      }
-      if (!ok) break;
-      commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
-      for (int j = 0; ok && j < it.n_max; ++j) {
-        bool v_ready = false, k_next_ready = false;
+    if constexpr (kSepP) {
+      uint32_t sn[2] = {0, 0};  // score MMAs issued for tile t (all items)
+      // S_t of K tile g once the softmax warps have read the previous S_t out of its columns.
+      auto issue_s_sep = [&](int t, uint32_t g, bool ready) -> bool {
+        if (sn[t] > 0 && !mbar_wait_warp(bar(L::bSFree + t), (sn[t] - 1) & 1, ctl)) return false;
+        ++sn[t];
+        return issue_s(t, g, ready);
+      };
+      for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+        const int k = fwd_item_index(r, p.num_items);
+        if (k < 0) continue;
+        const FwdItem it = fwd_item<kWin, kSplit>(k, p);
+        if (it.n_max == 0) continue;
+        bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (it.a[t] <= j && j < it.b[t]) {
-            if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
-            v_ready = true;
-          }
-          if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
-            if (!(ok = issue_s(t, gk + j + 1, k_next_ready))) break;
-            k_next_ready = true;
-            if (j + 2 == it.b[t]) commit(bar(L::bQEmpty + t));
+          if (!ok) break;
+          if (it.b[t] == it.a[t]) continue;
+          if (!(ok = mbar_wait_warp(bar(L::bQ + t), qn[t] & 1, ctl))) break;
+          ++qn[t];
+          tc_fence_after();
+          if (it.a[t] == 0) {  // score MMA of the item's first key tile
+            if (!(ok = issue_s_sep(t, gk, k_ready))) break;
+            k_ready = true;
+            if (it.b[t] == 1) commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
           }
         }
         if (!ok) break;
-        commit(bar(L::bVEmpty + (gv + j) % NV));
-        if (j + 1 < it.n_max) commit(bar(L::bKEmpty + (gk + j + 1) % NK));
+        commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          // Next scores first (they wait only for S_t to be read), then this step's P.V.
+          bool k_next_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
+              if (!(ok = issue_s_sep(t, gk + j + 1, k_next_ready))) break;
+              k_next_ready = true;
+              if (j + 2 == it.b[t]) commit(bar(L::bQEmpty + t));
+            }
+          }
+          if (!ok) break;
+          if (j + 1 < it.n_max) commit(bar(L::bKEmpty + (gk + j + 1) % NK));
+          bool v_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (it.a[t] <= j && j < it.b[t]) {
+              if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
+              v_ready = true;
+              commit(bar(L::bPFree + t));
+            }
+          }
+          if (!ok) break;
+          commit(bar(L::bVEmpty + (gv + j) % NV));
+        }
+        gk += it.n_max;
+        gv += it.n_max;
       }
-      gk += it.n_max;
-      gv += it.n_max;
+    } else {
+      for (int r = 0; ok && r * (int)gridDim.x < p.num_items; ++r) {
+        const int k = fwd_item_index(r, p.num_items);
+        if (k < 0) continue;
+        const FwdItem it = fwd_item<kWin, kSplit>(k, p);
+        if (it.n_max == 0) continue;
+        bool k_ready = false;
+  #pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          if (it.b[t] == it.a[t]) continue;
+          if (!(ok = mbar_wait_warp(bar(L::bQ + t), qn[t] & 1, ctl))) break;
+          ++qn[t];
+          tc_fence_after();
+          if (it.a[t] == 0) {  // score MMA of the item's first key tile
+            if (!(ok = issue_s(t, gk, k_ready))) break;
+            k_ready = true;
+            if (it.b[t] == 1) commit(bar(L::bQEmpty + t));  // Q_t's last score MMA
+          }
+        }
+        if (!ok) break;
+        commit(bar(L::bKEmpty + gk % NK));  // key tile 0 of the item: its score MMAs are issued
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          bool v_ready = false, k_next_ready = false;
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (it.a[t] <= j && j < it.b[t]) {
+              if (!(ok = issue_pv(t, gv + j, j == it.a[t], j + 1 == it.b[t], v_ready))) break;
+              v_ready = true;
+            }
+            if (it.a[t] <= j + 1 && j + 1 < it.b[t]) {
+              if (!(ok = issue_s(t, gk + j + 1, k_next_ready))) break;
+              k_next_ready = true;
+              if (j + 2 == it.b[t]) commit(bar(L::bQEmpty + t));
+            }
+          }
+          if (!ok) break;
+          commit(bar(L::bVEmpty + (gv + j) % NV));
+          if (j + 1 < it.n_max) commit(bar(L::bKEmpty + (gk + j + 1) % NK));
+        }
+        gk += it.n_max;
+        gv += it.n_max;
+      }
     }
     if (*abort_flag) {  // wait for issued MMAs before tensor memory is released
       if (elect_one()) {
@@ -402,6 +473,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + 128 * t + lane_off;
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
+    const uint32_t tP = kSepP ? tmem + kPCol + 128 * t + lane_off : tS;  // where P_t is written
     const float sl2 = p.scale_log2;
     uint32_t sc = 0;  // score tiles of this query tile processed so far (all items)
     uint32_t on = 0;  // items of this query tile whose output was completed
@@ -443,6 +515,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        if constexpr (kSepP) {  // S_t's columns may now take the next score MMA
+          tc_fence_before();
+          mbar_arrive(bar(L::bSFree + t));
+        }
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) mask32(sr[c], c * 32, lo, lim);
@@ -465,8 +541,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float pmx = ex2(fmaf(mx, sl2, -m_use));
           e_run = e_run * corr + (__uint_as_float(pack_bf16(pmx, 0.f) << 16) - pmx);
         }
-        // P = 2^(S*scale*log2e - m) as bf16 over the S columns (all already in registers), and
-        // the row sum.
+        if constexpr (kSepP) {
+          // The previous P.V of this tile has consumed P_t and updated O_t (before the first
+          // tile of an item that is the previous item's last P.V, already complete).
+          if (sc + j > 0 && !mbar_wait_warp(bar(L::bPFree + t), (sc + j - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // P = 2^(S*scale*log2e - m) as bf16 over the S columns (all already in registers), or
+        // into P_t's own columns in separate-P mode, and the row sum.
         float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m_use, -m_use);
@@ -480,11 +565,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             sum[(i >> 1) & 1] = add2(sum[(i >> 1) & 1], pp);
             pk[i >> 1] = pack_bf16(pp.x, pp.y);
           }
-          // P chunk c covers columns [16c, 16c+16).
-          tmem_st16(tS + c * 16, pk);
+          // P chunk c covers columns [16c, 16c+16) of tP.
+          tmem_st16(tP + c * 16, pk);
         }
-        // O += P_{j-1} V was issued before S_j and has completed with it; a rescale of O must
-        // land before this tile's P.V, which waits for the arrival below.
+        // O += P_{j-1} V has completed (it was issued before S_j, whose completion implies it,
+        // or, in separate-P mode, bPFree said so); a rescale of O must land before this tile's
+        // P.V, which waits for the arrival below.
         if (j > 0 && resc) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
