@@ -125,12 +125,13 @@ bool load_encoder() {
   return g_encode != nullptr;
 }
 
-// 3-D map over a [planes][N][d] bf16 tensor; box = 64 columns (128 B, one swizzle span) x 128
-// rows x 1 plane, 128-byte swizzle. Rows past N read as zero.
-int make_map(CUtensorMap* m, const void* base, int d, int N, long long planes) {
+// 3-D map over a [planes][N][d] bf16 tensor; box = 64 columns (128 B, one swizzle span) x
+// box_rows rows (128 unless given) x 1 plane, 128-byte swizzle. Rows past N read as zero (loads)
+// or are not written (stores).
+int make_map(CUtensorMap* m, const void* base, int d, int N, long long planes, int box_rows = fa::kTile) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)planes};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)fa::kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -257,14 +258,16 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   int num_sms = 0;
   FA_TRY(current_device(&status, &num_sms));
   if (!load_encoder()) return FA_ERR_LAUNCH;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
   FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
   FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
+  FA_TRY(make_map(&to, o, d, N, (long long)B * Hq, 32));  // O stores: 32 rows (one warp) per box
   fa::FwdLaunch a;
   a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;
+  a.tm_o = &to;
   a.o = o;
   a.lse = lse;
   a.counters = counters;

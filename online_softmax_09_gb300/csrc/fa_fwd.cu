@@ -138,7 +138,10 @@ struct FwdSmem {
   static constexpr int kQ = 0;  // Q0, Q1
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + NK * kTileBytes;
-  static constexpr int kBar = kV + NV * kTileBytes;
+  // O staging for the epilogue's bulk tensor stores: one 4 KB buffer (32 rows x 64 columns,
+  // 128-byte swizzled) per softmax warp.
+  static constexpr int kOStage = kV + NV * kTileBytes;
+  static constexpr int kBar = kOStage + 8 * 4096;
   // mbarrier indices
   static constexpr int bQ = 0;                // 2
   static constexpr int bKFull = bQ + 2;       // NK
@@ -190,7 +193,8 @@ __device__ __forceinline__ void mask32(uint32_t (&s)[32], int col0, int lo, int 
 template <int D, int NK, int NV, bool kWin, bool kSplit>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
   using L = FwdSmem<D, NK, NV>;
   // Separate-P mode (see the TMEM plan above) and the first TMEM column of P_0.
   constexpr bool kSepP = (D == 64);
@@ -241,6 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -475,6 +480,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tO = tmem + 256 + 128 * t + lane_off;
     const uint32_t tP = kSepP ? tmem + kPCol + 128 * t + lane_off : tS;  // where P_t is written
     const float sl2 = p.scale_log2;
+    const uint32_t o_stage = sbase + L::kOStage + (uint32_t)warp * 4096;  // this warp's O buffer
     uint32_t sc = 0;  // score tiles of this query tile processed so far (all items)
     uint32_t on = 0;  // items of this query tile whose output was completed
     bool ok = true;
@@ -638,14 +644,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // O_t has been read: the next item's first P.V may overwrite it.
       tc_fence_before();
       mbar_arrive(bar(L::bOFree + t));
-      if (row < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)itm.bh * p.N + row) * D);
+      // O leaves through shared memory: the warp writes its 32 rows of one 64-column chunk into
+      // its buffer (16-byte granule g of row r at g ^ (r mod 8), the 128-byte swizzle, so the
+      // writes are free of bank conflicts) and one lane stores the box with a bulk tensor store,
+      // which writes whole lines and leaves out rows past N. Storing each row from its own
+      // thread wrote 16 bytes into each of 32 rows per instruction.
+      const int y0 = qt * kTile + (warp & 3) * 32;  // this warp's first row
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+      for (int c = 0; c < D / 64 && y0 < p.N; ++c) {  // (a warp whose rows all lie past N stores nothing)
+        if (lane == 0) bulk_wait_read_all();  // the previous store from this buffer has read it
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[c * 4 + i] = w[c][i];
-        p.lse[(size_t)itm.bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
+        for (int g = 0; g < 8; ++g) {
+          const uint4 v4 = w[2 * c + (g >> 2)][g & 3];
+          st_shared_v4(o_stage + (uint32_t)lane * 128 + ((g ^ (lane & 7)) << 4), v4.x, v4.y, v4.z, v4.w);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_o, o_stage, c * 64, y0, itm.bh);
+          bulk_commit_group();
+        }
       }
+      if (row < p.N) p.lse[(size_t)itm.bh * p.N + row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
       if (!kSplit && p.counters != nullptr) {
         unsigned int r = n_raised;
 #pragma unroll
@@ -658,6 +679,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
   }
+
+  if (warp < 8 && lane == 0) bulk_wait_all();  // every O store has landed before the CTA exits
 
   // ------------------------------------------------------------------ teardown
   tc_fence_before();
@@ -676,7 +699,8 @@ static cudaError_t launch_fwd_mode(const FwdLaunch& a, const FwdParams& p) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
-  fa_fwd_kernel<D, NK, NV, kWin, kSplit><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+  fa_fwd_kernel<D, NK, NV, kWin, kSplit><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
+                                                                                  *a.tm_o, p);
   return cudaGetLastError();
 }
 
@@ -745,7 +769,9 @@ cudaError_t launch_fwd(const FwdLaunch& a) {
   p.split_len = (p.num_tiles + p.num_splits - 1) / p.num_splits;
   p.num_items = p.num_pairs * a.B * a.Hq * p.num_splits;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  cudaError_t e = (a.d == 128) ? launch_fwd_t<128, 3, 2>(a, p) : launch_fwd_t<64, 4, 4>(a, p);
+  // K and V rings: two stages each at d = 128 (a third K stage measured no faster, and its 32 KB
+  // now hold the O staging buffers), four each at d = 64.
+  cudaError_t e = (a.d == 128) ? launch_fwd_t<128, 2, 2>(a, p) : launch_fwd_t<64, 4, 4>(a, p);
   if (e != cudaSuccess || p.num_splits == 1) return e;
   const long long rows = (long long)a.B * a.Hq * a.N;
   const long long threads = rows * (a.d / 4);

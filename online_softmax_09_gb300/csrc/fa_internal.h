@@ -23,6 +23,7 @@ struct FwdLaunch {
   const CUtensorMap* tm_q;
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
+  const CUtensorMap* tm_o;  // O as [B*Hq][N][d], box 64 columns x 32 rows (epilogue stores)
   void* o;
   float* lse;
   unsigned long long* counters;  // nullable

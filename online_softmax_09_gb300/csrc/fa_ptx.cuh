@@ -115,6 +115,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bulk tensor store shared -> global of the box at tensor coordinates {x, y, z} of `map` (box
+// rows past the tensor's extent are not written). Completion is tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Plain bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
@@ -139,6 +148,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // All but the most recently committed bulk group have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_but1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Every committed bulk group has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Every committed bulk group has completed (its writes to global memory included).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
