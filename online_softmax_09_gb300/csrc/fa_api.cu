@@ -319,7 +319,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   int num_sms = 0;
   FA_TRY(current_device(&status, &num_sms));
   char* ws = static_cast<char*>(workspace);
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (stages & fa::kBwdCompute) {
     if (!load_encoder()) return FA_ERR_LAUNCH;
     FA_TRY(make_map(&tq, q, d, N, (long long)B * Hq));
@@ -327,8 +327,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
     FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
     FA_TRY(make_map(&tdo, dout, d, N, (long long)B * Hq));
     FA_TRY(make_map_dq(&tdq, ws + w.dq_acc, d, (long long)B * Hq * fa::round_up_tile(N)));
+    FA_TRY(make_map(&tdk, dk, d, N, (long long)B * Hkv, 32));  // dK, dV stores: 32 rows per box
+    FA_TRY(make_map(&tdv, dv, d, N, (long long)B * Hkv, 32));
   }
   fa::BwdLaunch a;
+  a.tm_dk = &tdk;
+  a.tm_dv = &tdv;
   a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;

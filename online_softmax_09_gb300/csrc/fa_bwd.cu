@@ -172,6 +172,8 @@ struct BwdSmem {
 };
 
 constexpr int kBwdThreads = 448;
+// CTAs of at most this many query tiles store dK and dV with bulk tensor stores (see the epilogue).
+constexpr int kBwdStoreViaTmaMaxIter = 32;
 // TMEM column of the packed bf16 P^T operand for the 16 queries of MMA step kk.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
 
@@ -179,7 +181,8 @@ template <int D, bool kWin>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                       const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -258,6 +261,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_dq);
+
   }
   tc_fence_before();
   __syncthreads();
@@ -533,24 +537,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok) ok = mbar_wait_warp(bar(L::bFinal), 0, ctl);
     if (ok) {
       tc_fence_after();
-      const size_t row_off = ((size_t)(b * p.Hkv + hkv) * p.N + key) * D;
       const uint32_t src = grp ? tdK : tdV;
       const float mul = grp ? p.scale : 1.f;
-      __nv_bfloat16* dst_base = grp ? p.dk : p.dv;
+      if (n_iter <= kBwdStoreViaTmaMaxIter) {
+        // A short CTA's epilogue is a noticeable part of its time: every MMA has completed, so the
+        // Q/dO stages are idle, and warp w of the dV (dK) warps writes its 32 key rows, one
+        // 64-column chunk at a time, into an 8 KB region of stage 0 (1) in the 128-byte swizzled
+        // order; one lane stores each chunk with a bulk tensor store (whole lines; rows past N are
+        // not written). Measured +9 % on the backward at N = 512 and +3.6 % at B=4 H=16 N=4096
+        // causal. A long CTA stores its rows directly and leaves the TMA unit to its dQ
+        // reductions (the same speed on CTAs of 128 query tiles; this build, with both paths,
+        // also ran ~2 % faster there than one with the bulk path alone).
+        const uint32_t buf = stage(grp) + (uint32_t)(warp & 3) * 8192;
+        const int y0 = n * kTile + (warp & 3) * 32;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(src + lane_off + c * 32, a);
-        tmem_ld_wait(a);
-        uint4 w[4];
-        uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t a[2][32];
+          tmem_ld32(src + lane_off + (2 * c) * 32, a[0]);
+          tmem_ld32(src + lane_off + (2 * c + 1) * 32, a[1]);
+          tmem_ld_wait(a[0]);
+          tmem_ld_wait(a[1]);
+          const uint32_t cb = buf + (uint32_t)c * 4096;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* v = a[g >> 2] + 8 * (g & 3);
+            st_shared_v4(cb + (uint32_t)lane * 128 + ((g ^ (lane & 7)) << 4),
+                         pack_bf16(__uint_as_float(v[0]) * mul, __uint_as_float(v[1]) * mul),
+                         pack_bf16(__uint_as_float(v[2]) * mul, __uint_as_float(v[3]) * mul),
+                         pack_bf16(__uint_as_float(v[4]) * mul, __uint_as_float(v[5]) * mul),
+                         pack_bf16(__uint_as_float(v[6]) * mul, __uint_as_float(v[7]) * mul));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && y0 < p.N) {
+            tma_store_3d(grp ? &tm_dk : &tm_dv, cb, c * 64, y0, b * p.Hkv + hkv);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_read_all();  // the stores have read their shared memory
+      } else {
+        const size_t row_off = ((size_t)(b * p.Hkv + hkv) * p.N + key) * D;
+        __nv_bfloat16* dst_base = grp ? p.dk : p.dv;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = w[j];
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(src + lane_off + c * 32, a);
+          tmem_ld_wait(a);
+          uint4 w[4];
+          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = w[j];
+          }
         }
       }
     }
@@ -682,7 +724,8 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     p.scale_log2 = a.scale * kLog2e;
     p.band = bwd_band(a.B, a.Hq, a.Hkv, a.N, D, a.causal, a.window, a.num_sms);
     const long long grid = (long long)a.B * a.Hkv * T;
-    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, p);
+    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, *a.tm_dk,
+                                                          *a.tm_dv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

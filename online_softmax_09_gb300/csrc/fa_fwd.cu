@@ -245,7 +245,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -680,7 +679,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   }
 
-  if (warp < 8 && lane == 0) bulk_wait_all();  // every O store has landed before the CTA exits
+  // Every O store has read its shared memory before the CTA releases it (the stores' writes to
+  // global memory complete by the end of the kernel).
+  if (warp < 8 && lane == 0) bulk_wait_read_all();
 
   // ------------------------------------------------------------------ teardown
   tc_fence_before();

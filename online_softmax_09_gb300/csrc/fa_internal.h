@@ -45,6 +45,8 @@ struct BwdLaunch {
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_do;
   const CUtensorMap* tm_dq;  // fp32 dQ accumulator viewed as [B*Hq*Npad][d], box 32 x 32
+  const CUtensorMap* tm_dk;  // dK, dV as [B*Hkv][N][d], box 64 columns x 32 rows (epilogue stores)
+  const CUtensorMap* tm_dv;
   const void* o;
   const void* dout;
   const float* lse;
