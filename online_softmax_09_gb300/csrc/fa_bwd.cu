@@ -30,7 +30,8 @@
 // Warp roles of the main kernel: 0-3 and 10-13 softmax/dS (thread = key row; warps 0-3 take
 // query columns [0, 64) of every row, warps 10-13 columns [64, 128), so each row's elementwise
 // work is split between two warps of the same TMEM lane quarter), then the final dV (0-3) and
-// dK (10-13) epilogue; 4 TMA producer, 5 MMA issuer and TMEM owner, 6-9 dQ drain.
+// dK (10-13) epilogue; 4 TMA producer, 5 MMA issuer (the whole warp runs the loop, one elected
+// lane issues) and TMEM owner, 6-9 dQ drain.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 // P^T is packed bf16 (two queries per column): queries [0, 64) in columns [0, 32), queries
 // [64, 128) in [64, 96), i.e. each half over score columns its own warps have already read.

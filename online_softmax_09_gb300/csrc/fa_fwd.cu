@@ -6,17 +6,18 @@
 // previous item's epilogue is still writing O. Roles:
 //   warp 8      TMA producer: Q0, Q1 once, then K_j into an NK-stage ring and V_j into an
 //               NV-stage ring.
-//   warp 9      MMA issuer (one thread) and TMEM owner. Issue order per key tile j:
+//   warp 9      MMA issuer and TMEM owner: the whole warp runs the issue loop (warp-uniform
+//               indices and descriptors) and one elected lane issues. Issue order per key tile j:
 //                 O0 += P0_j V_j, S0_{j+1} = Q0 K_{j+1}^T, O1 += P1_j V_j, S1_{j+1} = Q1 K_{j+1}^T
 //               so that while one softmax warpgroup turns S into P, the tensor core works on
-//               the other tile.
+//               the other tile (separate-P mode below: both S_{j+1} first, then both P.V).
 //   warps 0-3   softmax warpgroup of tile 0, warps 4-7 of tile 1: one thread per query row,
 //               running max m and sum l ("FlashAttention Implementation > How FlashAttention
 //               Uses Tiling", "The Running Statistics"), correction exp(m_old - m_new) applied
 //               to l and to the output accumulator in TMEM ("Why the Correction Factor
 //               Works"), P = exp(S - m) written back to TMEM as bf16 over the S columns, and
 //               the epilogue O = acc / l, LSE = m + ln l ("LLM Architecture Refresh [3]",
-//               section 4).
+//               section 4), O leaving through a per-warp shared buffer and bulk tensor stores.
 // Causal: key tiles after a query tile are never loaded or computed (same post, section 7);
 // the diagonal tile and a ragged last tile are masked element-wise.
 //
