@@ -139,6 +139,19 @@ int make_map(CUtensorMap* m, const void* base, int d, int N, long long planes, i
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
 }
 
+// 3-D map over split-KV partial outputs [planes][N][d] fp32; box = 32 columns (128 B) x 32 rows
+// x 1 plane, 128-byte swizzle (the staging layout of the forward's epilogue stores).
+int make_map_part(CUtensorMap* m, void* base, int d, int N, long long planes) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * (cuuint64_t)d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
+}
+
 // 2-D map over the fp32 dQ accumulator [rows][d]; box = 32 columns (128 B) x 32 rows,
 // 128-byte swizzle (the staging layout the backward's dQ drain writes).
 int make_map_dq(CUtensorMap* m, void* base, int d, long long rows) {
@@ -263,11 +276,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   FA_TRY(make_map(&tk, k, d, N, (long long)B * Hkv));
   FA_TRY(make_map(&tv, v, d, N, (long long)B * Hkv));
   FA_TRY(make_map(&to, o, d, N, (long long)B * Hq, 32));  // O stores: 32 rows (one warp) per box
+  CUtensorMap tp = to;  // split-KV partial outputs (fp32); unused without splits
+  if (num_splits > 1) FA_TRY(make_map_part(&tp, o_part, d, N, (long long)num_splits * B * Hq));
   fa::FwdLaunch a;
   a.tm_q = &tq;
   a.tm_k = &tk;
   a.tm_v = &tv;
   a.tm_o = &to;
+  a.tm_opart = &tp;
   a.o = o;
   a.lse = lse;
   a.counters = counters;

@@ -195,7 +195,7 @@ template <int D, int NK, int NV, bool kWin, bool kSplit>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_opart, const FwdParams p) {
   using L = FwdSmem<D, NK, NV>;
   // Separate-P mode (see the TMEM plan above) and the first TMEM column of P_0.
   constexpr bool kSepP = (D == 64);
@@ -608,19 +608,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (kSplit && split_count(qt, p) > 1) {
         // Split mode: the partial output acc / l (fp32) and its LSE, merged later. (A tile whose
         // keys all fall in one split gets its final O and LSE below, as without splits.)
+        // The partial rows go out like O below, 32 fp32 columns (a 4 KB box) at a time.
         if (row < p.N) p.lse_part[part_row] = (m_run + lg2(l_run)) * 0.6931471805599453f;
-        float4* dst = reinterpret_cast<float4*>(p.o_part + part_row * D);
+        const int y0 = qt * kTile + (warp & 3) * 32;
+        const int zp = itm.split * p.B * p.Hq + itm.bh;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait(o);
-          if (row < p.N) {
+          if (y0 < p.N) {
+            if (lane == 0) bulk_wait_read_all();  // the previous store from this buffer has read it
+            __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                           __uint_as_float(o[4 * i + 2]) * inv_l,
-                                           __uint_as_float(o[4 * i + 3]) * inv_l);
+            for (int g = 0; g < 8; ++g)
+              st_shared_v4(o_stage + (uint32_t)lane * 128 + ((g ^ (lane & 7)) << 4),
+                           __float_as_uint(__uint_as_float(o[4 * g]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * g + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * g + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(o[4 * g + 3]) * inv_l));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tm_opart, o_stage, c * 32, y0, zp);
+              bulk_commit_group();
+            }
           }
         }
         tc_fence_before();
@@ -702,7 +714,7 @@ static cudaError_t launch_fwd_mode(const FwdLaunch& a, const FwdParams& p) {
   if (e != cudaSuccess) return e;
   const int grid = p.num_items < a.num_sms ? p.num_items : a.num_sms;
   fa_fwd_kernel<D, NK, NV, kWin, kSplit><<<grid, kFwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v,
-                                                                                  *a.tm_o, p);
+                                                                                  *a.tm_o, *a.tm_opart, p);
   return cudaGetLastError();
 }
 

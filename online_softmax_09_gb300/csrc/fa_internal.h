@@ -24,6 +24,7 @@ struct FwdLaunch {
   const CUtensorMap* tm_k;
   const CUtensorMap* tm_v;
   const CUtensorMap* tm_o;  // O as [B*Hq][N][d], box 64 columns x 32 rows (epilogue stores)
+  const CUtensorMap* tm_opart;  // split-KV partials as [splits*B*Hq][N][d] fp32, box 32 x 32
   void* o;
   float* lse;
   unsigned long long* counters;  // nullable
