@@ -119,7 +119,8 @@ int fa_fwd_stats(const void *q, const void *k, const void *v, void *o, float *ls
 
 /*
  * Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator, the per-row
- * delta = rowsum(dO * O) and the base-2 LSE, each over rows padded to a multiple of 128.
+ * delta = rowsum(dO * O) and the base-2 LSE, each over rows padded to a multiple of 128,
+ * and 256 bytes for the compute stage's work-item counter.
  * Grows as O(B * Hq * N * d): never with N^2. Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
@@ -159,10 +160,12 @@ int fa_bwd_window(const void *q, const void *k, const void *v, const void *o, co
  * fa_bwd(...) is exactly prepare, compute, finalize.
  *   fa_bwd_prepare : -delta = -rowsum(dout * o) and -lse * log2(e) per query row into the
  *                    workspace (negated for the compute kernel's packed arithmetic), and
- *                    zeroes the workspace's fp32 dQ accumulator
+ *                    zeroes the workspace's fp32 dQ accumulator and work-item counter
  *                    (memory-bound: reads o, dout, lse).
  *   fa_bwd_compute : the recompute kernel: writes dk, dv and adds dQ contributions (before
  *                    the final scale) into the workspace accumulator (reads q, k, v, dout).
+ *                    It leaves the counter at zero, so it may be run again (to time it
+ *                    alone, say); dq is right only for one compute after each prepare.
  *   fa_bwd_finalize: dq = bf16(scale * accumulator).
  * Same argument meanings, layouts and errors as fa_bwd.
  */

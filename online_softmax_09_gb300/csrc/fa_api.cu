@@ -184,7 +184,7 @@ int check_ptr(const void* p) {
 float resolve_scale(float scale, int d) { return (scale > 0.f) ? scale : 1.0f / std::sqrt((float)d); }
 
 struct WorkspaceLayout {
-  size_t dq_acc, delta, lse2, total;
+  size_t dq_acc, delta, lse2, next_item, total;
 };
 WorkspaceLayout workspace_layout(int B, int Hq, int N, int d) {
   const size_t rows = (size_t)B * Hq * fa::round_up_tile(N);
@@ -193,7 +193,8 @@ WorkspaceLayout workspace_layout(int B, int Hq, int N, int d) {
   w.dq_acc = 0;
   w.delta = up(rows * d * 4);
   w.lse2 = w.delta + up(rows * 4);
-  w.total = w.lse2 + up(rows * 4);
+  w.next_item = w.lse2 + up(rows * 4);
+  w.total = w.next_item + 256;
   return w;
 }
 
@@ -363,6 +364,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.next_item = reinterpret_cast<uint32_t*>(ws + w.next_item);
   a.status = status;
   a.B = B;
   a.Hq = Hq;

@@ -9,10 +9,11 @@
 //
 // Three kernels on the caller's stream:
 //   1. preprocess: -delta and -LSE*log2(e) per query row (padded rows: 0 and -inf), and
-//      zeroes the fp32 dQ accumulator.                                         (HBM-bound)
-//   2. main: one CTA per (batch, kv head, 128-key tile). It keeps K_n and V_n in shared
-//      memory and the dK, dV accumulators in TMEM, and loops over the G query heads of its
-//      group and their query tiles (causal: from the diagonal tile on). Per query tile i:
+//      zeroes the fp32 dQ accumulator and the main kernel's work counter.     (HBM-bound)
+//   2. main: persistent, one CTA per SM walking work items, one item per (batch, kv head,
+//      128-key tile). For an item it keeps K_n and V_n in shared memory and the dK, dV
+//      accumulators in TMEM, and loops over the G query heads of its group and their query
+//      tiles (causal: from the diagonal tile on). Per query tile i:
 //        softmax warps (thread = key row): P_i^T = 2^(S_i^T scale log2e - LSE2), bf16 -> TMEM
 //        MMA  dV += P_i^T dO_i ;  dP_i^T = V_n dO_i^T ;  S_{i+1}^T = K_n Q_{i+1}^T
 //        softmax warps: dS_i^T = P_i^T (dP_i^T - delta), bf16 -> shared memory
@@ -22,16 +23,20 @@
 //      The next tile's S^T is computed while the softmax warps work on dS_i, and its P while
 //      the dQ and dK MMAs run, so the tensor core does not wait for the softmax warps. The one
 //      shared-memory copy of dS serves both of its MMAs (MN-major A of dQ, K-major A of dK),
-//      and dQ goes first so that its drain overlaps the dK MMA. CTAs are launched in bands of
+//      and dQ goes first so that its drain overlaps the dK MMA. Items are numbered in bands of
 //      (batch, kv head) pairs, key tile by key tile within a band, so that the Q, dO and dQ
-//      accumulator rows that a band's CTAs share stay in L2 (see bwd_band).
+//      accumulator rows that a band's items share stay in L2 (see bwd_band), and handed out
+//      in that order from a counter as CTAs finish their previous item. An item's end overlaps
+//      the next one's start: its V tile loads once its last dP^T MMA has read V, the next
+//      item's first dP^T and the softmax warps' next P phase run while the drain warps write
+//      dK and dV out.
 //   3. dQ conversion: dq = bf16(scale * accumulator).
 //
 // Warp roles of the main kernel: 0-3 and 10-13 softmax/dS (thread = key row; warps 0-3 take
 // query columns [0, 64) of every row, warps 10-13 columns [64, 128), so each row's elementwise
-// work is split between two warps of the same TMEM lane quarter), then the final dV (0-3) and
-// dK (10-13) epilogue; 4 TMA producer, 5 MMA issuer (the whole warp runs the loop, one elected
-// lane issues) and TMEM owner, 6-9 dQ drain.
+// work is split between two warps of the same TMEM lane quarter); 4 TMA producer and work
+// fetcher, 5 MMA issuer (the whole warp runs the loop, one elected lane issues) and TMEM owner,
+// 6-9 dQ drain and, at the end of each item, the dV and dK epilogue.
 // TMEM columns: S^T/P^T [0,128), dP^T/dQ [128,256), dV [256,256+D), dK [256+D,256+2D).
 // P^T is packed bf16 (two queries per column): queries [0, 64) in columns [0, 32), queries
 // [64, 128) in [64, 96), i.e. each half over score columns its own warps have already read.
@@ -55,11 +60,13 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          const float* __restrict__ lse, float* __restrict__ dq_acc,
                                                          float* __restrict__ delta, float* __restrict__ lse2,
-                                                         int N, int Npad, long long rows) {
+                                                         uint32_t* __restrict__ next_item, int N, int Npad,
+                                                         long long rows) {
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 bytes) each
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long r = gt / TPR;  // row of the padded [B*Hq][Npad] grid
   const int part = (int)(gt % TPR);
+  if (gt == 0) next_item[0] = next_item[1] = 0u;  // the main kernel's work-item counters
   if (r >= rows) return;  // rows are whole TPR-lane groups, so groups exit together
   const long long bh = r / Npad;
   const int n = (int)(r - bh * Npad);
@@ -126,8 +133,41 @@ struct BwdParams {
   int B, Hq, Hkv, N, Npad, causal, num_tiles;
   int window;  // > 0: causal sliding window of this many keys
   float scale, scale_log2;
-  int band;  // (b, kv head) pairs per launch band; B * Hkv for a single band
+  int band;       // (b, kv head) pairs per launch band; B * Hkv for a single band
+  int num_items;  // B * Hkv * num_tiles work items (key tiles)
+  uint32_t* next_item;  // workspace: [0] items handed out beyond the first gridDim.x,
+                        // [1] CTAs that found no more items
 };
+
+// Work item `idx`: key tile n of kv head (b, hkv). Items are numbered band by band (p.band
+// consecutive (b, kv head) pairs, the last band possibly narrower) and key tile by key tile
+// within a band, so a band's causal tiles with the most query tiles come first and its Q, dO
+// and dQ accumulator rows stay in L2 while its items run. The item visits the G query heads of
+// its group and, per head, query tiles [i0, i0 + n_i): from the diagonal (causal) to, with a
+// sliding window, the tile of the last query within `window` of the tile's last key.
+struct BwdItem {
+  int b, hkv, n, i0, n_i, n_iter;
+};
+template <bool kWin>
+__device__ __forceinline__ BwdItem bwd_item(int idx, const BwdParams& p) {
+  BwdItem w;
+  const int BHk = p.B * p.Hkv;
+  const int per_band = p.band * p.num_tiles;
+  const int band_i = idx / per_band;
+  const int first = band_i * p.band;
+  const int width = min(p.band, BHk - first);
+  const int local = idx - band_i * per_band;
+  w.n = local / width;
+  const int bhk = first + (local - w.n * width);
+  w.b = bhk / p.Hkv;
+  w.hkv = bhk - w.b * p.Hkv;
+  w.i0 = p.causal ? w.n : 0;
+  const int i_end =
+      kWin ? min(p.num_tiles, (w.n * kTile + kTile - 1 + p.window - 1) / kTile + 1) : p.num_tiles;
+  w.n_i = i_end - w.i0;
+  w.n_iter = (p.Hq / p.Hkv) * w.n_i;
+  return w;
+}
 
 template <int D>
 struct BwdSmem {
@@ -147,24 +187,33 @@ struct BwdSmem {
   static constexpr int kDQ = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
   static constexpr int kBar = kDQ + 4 * 2 * 32 * 128;
   enum {
-    bKV = 0,
-    bQFull = 1,       // 2
-    bDOFull = 3,      // 2
-    bStageEmpty = 5,  // 2
-    bSFull = 7,
+    bK = 0,
+    bV,
+    bQFull,           // 2
+    bDOFull = 4,      // 2
+    bStageEmpty = 6,  // 2
+    bSFull = 8,
     bDPFull,
     bPReady,
     bSmemDS,
     bDVDone,  // dV_i has finished reading dO_i (whose slot then takes dS_i)
     bDQFull,
     bDQFree,
-    bFinal,
-    bDrain,
+    bFinal,   // every MMA of the item has completed: dK, dV final in TMEM, K no longer read
+    bVFree,   // the item's last dP^T MMA has read V
+    bAccFree, // the epilogue has read dK and dV out of TMEM
+    bItemFull = 18,   // 2
+    bItemEmpty = 20,  // 2
+    bDrain = 22,
     kNumBars
   };
+  static_assert(bDOFull == bQFull + 2 && bStageEmpty == bDOFull + 2 && bSFull == bStageEmpty + 2 &&
+                    bItemEmpty == bItemFull + 2 && bDrain == bItemEmpty + 2,
+                "two-slot barriers overlap");
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kItem = kAbort + 4;  // 2 slots: work item index, -1 past the end
+  static constexpr int kBytes = kItem + 8;
   // No alignment slack: the kernel uses no static shared memory, so the dynamic window starts
   // on a 1024-byte boundary; the kernel checks this and stops (status 2) if it ever does not.
   static constexpr int kAlloc = kBytes;
@@ -173,8 +222,8 @@ struct BwdSmem {
 };
 
 constexpr int kBwdThreads = 448;
-// CTAs of at most this many query tiles store dK and dV with bulk tensor stores (see the epilogue).
-constexpr int kBwdStoreViaTmaMaxIter = 32;
+// Arrivals that release an item slot: the MMA warp, eight softmax warps and four drain warps.
+constexpr int kItemConsumers = 13;
 // TMEM column of the packed bf16 P^T operand for the 16 queries of MMA step kk.
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); }
 
@@ -206,39 +255,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: key tile n of kv head (b, hkv). CTAs are numbered band by band (p.band
-  // consecutive (b, kv head) pairs, the last band possibly narrower) and key tile by key tile
-  // within a band, so a band's causal tiles with the most query tiles start first and its
-  // Q, dO and dQ accumulator rows stay in L2 while its CTAs run.
-  const int BHk = p.B * p.Hkv;
-  const int per_band = p.band * p.num_tiles;
-  const int band_i = blockIdx.x / per_band;
-  const int first = band_i * p.band;
-  const int width = min(p.band, BHk - first);
-  const int local = blockIdx.x - band_i * per_band;
-  const int n = local / width;
-  const int bhk = first + (local - n * width);
-  const int b = bhk / p.Hkv;
-  const int hkv = bhk - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
-  // Query tiles that see key tile n: from the diagonal (causal) to, with a sliding window, the
-  // tile of the last query within `window` of the tile's last key.
-  const int i0 = p.causal ? n : 0;
-  const int i_end = kWin ? min(p.num_tiles, (n * kTile + kTile - 1 + p.window - 1) / kTile + 1) : p.num_tiles;
-  const int n_i = i_end - i0;
-  const int n_iter = G * n_i;
-  auto item = [&](int it, int& hq, int& i) {
-    const int g = it / n_i;
-    hq = hkv * G + g;
-    i = i0 + (it - g * n_i);
-  };
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItem);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::bKV), 1);
+    mbar_init(bar(L::bK), 1);
+    mbar_init(bar(L::bV), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(L::bQFull + s), 1);
       mbar_init(bar(L::bDOFull + s), 1);
       mbar_init(bar(L::bStageEmpty + s), 1);
+      mbar_init(bar(L::bItemFull + s), 1);
+      mbar_init(bar(L::bItemEmpty + s), kItemConsumers);
     }
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bDPFull), 1);
@@ -248,6 +276,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bDVDone), 1);
     mbar_init(bar(L::bDQFree), 128);
     mbar_init(bar(L::bFinal), 1);
+    mbar_init(bar(L::bVFree), 1);
+    mbar_init(bar(L::bAccFree), 128);
     mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -273,43 +303,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tdV = tmem + 256;
   const uint32_t tdK = tmem + 256 + D;
 
+  // Item r of this CTA, consumer side: waits until the producer has published it, reads it and
+  // releases the slot (one arrival per consumer warp). -1: no more items, or an abort.
+  auto take_item = [&](int r) -> int {
+    if (!mbar_wait_warp(bar(L::bItemFull + (r & 1)), (r >> 1) & 1, ctl)) return -1;
+    const int idx = item_slot[r & 1];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bItemEmpty + (r & 1)));
+    return idx;
+  };
+
   if (warp == 4) {
     // ------------------------------------------------------------------ TMA producer
+    // Persistent: the CTA's first item is blockIdx.x, later ones come from a workspace counter
+    // in launch order, so items still start in the order a one-CTA-per-item launch would start
+    // them (and the band order holds). Each item is published to the other roles through a
+    // two-slot ring. V of the next item is loaded once the previous item's last dP^T MMA has
+    // read V, K once all its MMAs are done; Q, dO, LSE2 and delta go through the two stages.
     if (lane == 0) {
       constexpr uint32_t kTB = L::kTileBytes;
-      const int kv_z = b * p.Hkv + hkv;
-      mbar_expect_tx(bar(L::bKV), 2 * kTB);
+      int g = 0;        // query tiles loaded so far (all items)
+      int issued = 0;   // tiles whose loads were issued
+      int r = 0;        // items published
+      int v_loads = 0, k_loads = 0;  // items whose V / K loads were issued
+      bool ok = true;
+      for (;; ++r) {
+        int idx = (r == 0) ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(p.next_item, 1u);
+        if (idx >= p.num_items) {
+          idx = -1;
+          // The last CTA to run out of items puts the counters back to zero (no CTA fetches
+          // again), so that the kernel can run again without a new prepare pass.
+          if (r > 0 && atomicAdd(p.next_item + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.next_item, 0u);
+            atomicExch(p.next_item + 1, 0u);
+          }
+        }
+        if (r >= 2 && !(ok = mbar_wait(bar(L::bItemEmpty + (r & 1)), ((r >> 1) - 1) & 1, ctl))) break;
+        item_slot[r & 1] = idx;
+        mbar_arrive(bar(L::bItemFull + (r & 1)));
+        if (idx < 0) break;
+        const BwdItem w = bwd_item<kWin>(idx, p);
+        const int kv_z = w.b * p.Hkv + w.hkv;
+        auto load_tile = [&](int it) -> bool {
+          const int s = g & 1;
+          if (!mbar_wait(bar(L::bStageEmpty + s), ((g >> 1) & 1) ^ 1, ctl)) return false;
+          const int gi = it / w.n_i;
+          const int hq = w.hkv * G + gi;
+          const int i = w.i0 + (it - gi * w.n_i);
+          const int qz = w.b * p.Hq + hq;
+          const size_t srow = (size_t)qz * p.Npad + (size_t)i * kTile;
+          const uint32_t st = stage(s);
+          mbar_expect_tx(bar(L::bQFull + s), kTB + 512);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sK + c * 16384, &tm_k, bar(L::bKV), c * 64, n * kTile, kv_z);
-        tma_load_3d(sV + c * 16384, &tm_v, bar(L::bKV), c * 64, n * kTile, kv_z);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_iter; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(bar(L::bStageEmpty + s), ((it >> 1) & 1) ^ 1, ctl)) break;
-        int hq, i;
-        item(it, hq, i);
-        const int qz = b * p.Hq + hq;
-        const size_t srow = (size_t)qz * p.Npad + (size_t)i * kTile;
-        const uint32_t st = stage(s);
-        mbar_expect_tx(bar(L::bQFull + s), kTB + 512);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(st + L::kStQ + c * 16384, &tm_q, bar(L::bQFull + s), c * 64, i * kTile, qz);
+          bulk_load(st + L::kStL, p.lse2 + srow, 512, bar(L::bQFull + s));
+          mbar_expect_tx(bar(L::bDOFull + s), kTB + 512);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(st + L::kStDO + c * 16384, &tm_do, bar(L::bDOFull + s), c * 64, i * kTile, qz);
+          bulk_load(st + L::kStD, p.delta + srow, 512, bar(L::bDOFull + s));
+          ++g;
+          issued = g;
+          return true;
+        };
+        // V (its slot frees first), the first query tile, then K.
+        if (r > 0 && !(ok = mbar_wait(bar(L::bVFree), (r - 1) & 1, ctl))) break;
+        mbar_expect_tx(bar(L::bV), kTB);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(st + L::kStQ + c * 16384, &tm_q, bar(L::bQFull + s), c * 64, i * kTile, qz);
-        bulk_load(st + L::kStL, p.lse2 + srow, 512, bar(L::bQFull + s));
-        mbar_expect_tx(bar(L::bDOFull + s), kTB + 512);
+          tma_load_3d(sV + c * 16384, &tm_v, bar(L::bV), c * 64, w.n * kTile, kv_z);
+        v_loads = r + 1;
+        if (w.n_iter > 0 && !(ok = load_tile(0))) break;
+        if (r > 0 && !(ok = mbar_wait(bar(L::bFinal), (r - 1) & 1, ctl))) break;
+        mbar_expect_tx(bar(L::bK), kTB);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(st + L::kStDO + c * 16384, &tm_do, bar(L::bDOFull + s), c * 64, i * kTile, qz);
-        bulk_load(st + L::kStD, p.delta + srow, 512, bar(L::bDOFull + s));
-        issued = it + 1;
+          tma_load_3d(sK + c * 16384, &tm_k, bar(L::bK), c * 64, w.n * kTile, kv_z);
+        k_loads = r + 1;
+        for (int it = 1; ok && it < w.n_iter; ++it) ok = load_tile(it);
+        if (!ok) break;
       }
-      if (*abort_flag) {
-        drain_wait(bar(L::bKV), 0);
-        for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
-          drain_wait(bar(L::bQFull + (it & 1)), (it >> 1) & 1);
-          drain_wait(bar(L::bDOFull + (it & 1)), (it >> 1) & 1);
+      if (!ok || *abort_flag) {
+        // Let the copies in flight land before the CTA releases its shared memory.
+        if (k_loads > 0) drain_wait(bar(L::bK), (k_loads - 1) & 1);
+        if (v_loads > 0) drain_wait(bar(L::bV), (v_loads - 1) & 1);
+        for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t) {
+          drain_wait(bar(L::bQFull + (t & 1)), (t >> 1) & 1);
+          drain_wait(bar(L::bDOFull + (t & 1)), (t >> 1) & 1);
         }
       }
     }
@@ -332,8 +413,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dDS_k = sdesc_sw128(sDS(0), 16, 1024), dDS_mn = sdesc_sw128(sDS(0), 16384, 1024);
     constexpr uint32_t kStage16 = L::kStageBytes >> 4;
     auto kmajor = [](int kk) -> uint32_t { return (uint32_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
-    auto issue_s = [&](int it) {  // S^T = K_n Q_it^T into tS
-      const uint64_t q = dSt_k + (uint32_t)((it & 1) * kStage16 + (L::kStQ >> 4));
+    // Tiles are counted over all items of the CTA (t), which sets every barrier phase.
+    auto issue_s = [&](int t) {  // S^T = K_n Q_t^T into tS
+      const uint64_t q = dSt_k + (uint32_t)((t & 1) * kStage16 + (L::kStQ >> 4));
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tS, dK_k + kmajor(kk), q + kmajor(kk), idSS, kk > 0);
@@ -341,13 +423,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
     };
-    // dP^T_it = V_n dO_it^T into tdP, once dO_it has landed and dQ_{it-1} has been drained
-    // out of these columns.
-    auto issue_dp = [&](int it) -> bool {
-      if (!mbar_wait_warp(bar(L::bDOFull + (it & 1)), (it >> 1) & 1, ctl)) return false;
-      if (it > 0 && !mbar_wait_warp(bar(L::bDQFree), (it - 1) & 1, ctl)) return false;
+    // dP^T_t = V_n dO_t^T into tdP, once dO_t has landed and dQ_{t-1} has been drained out of
+    // these columns.
+    auto issue_dp = [&](int t) -> bool {
+      if (!mbar_wait_warp(bar(L::bDOFull + (t & 1)), (t >> 1) & 1, ctl)) return false;
+      if (t > 0 && !mbar_wait_warp(bar(L::bDQFree), (t - 1) & 1, ctl)) return false;
       tc_fence_after();
-      const uint64_t dO = dSt_k + (uint32_t)((it & 1) * kStage16 + (L::kStDO >> 4));
+      const uint64_t dO = dSt_k + (uint32_t)((t & 1) * kStage16 + (L::kStDO >> 4));
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tdP, dV_k + kmajor(kk), dO + kmajor(kk), idSS, kk > 0);
@@ -356,61 +438,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait_warp(bar(L::bKV), 0, ctl) && mbar_wait_warp(bar(L::bQFull), 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      ok = n_iter > 0 && issue_dp(0);
-    }
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it & 1;
-      const uint32_t st16 = (uint32_t)s * kStage16;
-      // dV += P^T dO_i  (P^T from TMEM; dO as the MN-major B operand; dO_i waited for dP_i)
-      if (!(ok = mbar_wait_warp(bar(L::bPReady), it & 1, ctl))) break;
-      tc_fence_after();
-      {
-        const uint64_t dO = dSt_mn + st16 + (L::kStDO >> 4);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tdV, tS + packed_col(kk), dO + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
-          mma_commit(bar(L::bDVDone));
-        }
-        __syncwarp();
-      }
-      // S^T of the next query tile (P_i^T in these columns was read by the dV MMA above).
-      if (it + 1 < n_iter) {
-        if (!(ok = mbar_wait_warp(bar(L::bQFull + (s ^ 1)), ((it + 1) >> 1) & 1, ctl))) break;
-        tc_fence_after();
-        issue_s(it + 1);
-      }
-      // dQ_i = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns, first,
-      // so the drain starts as early as possible; then dK += dS^T Q_i with the same
-      // shared-memory dS as the K-major A operand.
-      if (!(ok = mbar_wait_warp(bar(L::bSmemDS), it & 1, ctl))) break;
-      tc_fence_after();
-      {
-        const uint32_t ds16 = L::kAliasDS ? st16 + (L::kStDO >> 4) : 0u;
-        const uint64_t ds_mn = (L::kAliasDS ? dSt_mn : dDS_mn) + ds16;
-        const uint64_t ds_k = (L::kAliasDS ? dSt_k : dDS_k) + ds16;
-        const uint64_t q_mn = dSt_mn + st16 + (L::kStQ >> 4);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tdP, ds_mn + (uint32_t)(kk * (2048 >> 4)), dK_mn + (uint32_t)(kk * (2048 >> 4)), idDQ, kk > 0);
-          mma_commit(bar(L::bDQFull));
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tdK, ds_k + kmajor(kk), q_mn + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
-          mma_commit(bar(L::bStageEmpty + s));
-        }
-        __syncwarp();
-      }
-      if (it + 1 < n_iter && !(ok = issue_dp(it + 1))) break;
-    }
-    if (ok) {
-      if (elect_one()) mma_commit(bar(L::bFinal));
+    auto commit = [&](int b_) {
+      if (elect_one()) mma_commit(bar(b_));
       __syncwarp();
+    };
+    bool ok = true;
+    int g = 0;  // query tiles of earlier items
+    for (int r = 0; ok; ++r) {
+      const int idx = take_item(r);
+      if (idx < 0) break;
+      const int n_iter = bwd_item<kWin>(idx, p).n_iter;  // >= 1: the diagonal tile always sees its keys
+      // The item's first dP^T needs V only (loaded as soon as the previous item's last dP^T read
+      // V); its first S^T waits for K, which follows the previous item's last MMAs.
+      ok = mbar_wait_warp(bar(L::bV), r & 1, ctl) && issue_dp(g);
+      if (ok && n_iter == 1) commit(L::bVFree);
+      ok = ok && mbar_wait_warp(bar(L::bK), r & 1, ctl) && mbar_wait_warp(bar(L::bQFull + (g & 1)), (g >> 1) & 1, ctl);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(g);
+      for (int it = 0; it < n_iter; ++it) {
+        const int t = g + it;
+        const int s = t & 1;
+        const uint32_t st16 = (uint32_t)s * kStage16;
+        // dV += P^T dO_t (P^T from TMEM; dO as the MN-major B operand; dO_t waited for dP_t).
+        // The item's first dV (and dK) overwrite the accumulators: the previous item's epilogue
+        // must have read them out.
+        if (!(ok = mbar_wait_warp(bar(L::bPReady), t & 1, ctl))) break;
+        if (it == 0 && r > 0 && !(ok = mbar_wait_warp(bar(L::bAccFree), (r - 1) & 1, ctl))) break;
+        tc_fence_after();
+        {
+          const uint64_t dO = dSt_mn + st16 + (L::kStDO >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tdV, tS + packed_col(kk), dO + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
+            mma_commit(bar(L::bDVDone));
+          }
+          __syncwarp();
+        }
+        // S^T of the next query tile (P_t^T in these columns was read by the dV MMA above).
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait_warp(bar(L::bQFull + (s ^ 1)), ((t + 1) >> 1) & 1, ctl))) break;
+          tc_fence_after();
+          issue_s(t + 1);
+        }
+        // dQ_t = dS K_n (dS and K both MN-major in shared memory) into the dP^T columns, first,
+        // so the drain starts as early as possible; then dK += dS^T Q_t with the same
+        // shared-memory dS as the K-major A operand.
+        if (!(ok = mbar_wait_warp(bar(L::bSmemDS), t & 1, ctl))) break;
+        tc_fence_after();
+        {
+          const uint32_t ds16 = L::kAliasDS ? st16 + (L::kStDO >> 4) : 0u;
+          const uint64_t ds_mn = (L::kAliasDS ? dSt_mn : dDS_mn) + ds16;
+          const uint64_t ds_k = (L::kAliasDS ? dSt_k : dDS_k) + ds16;
+          const uint64_t q_mn = dSt_mn + st16 + (L::kStQ >> 4);
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tdP, ds_mn + (uint32_t)(kk * (2048 >> 4)), dK_mn + (uint32_t)(kk * (2048 >> 4)), idDQ,
+                     kk > 0);
+            mma_commit(bar(L::bDQFull));
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tdK, ds_k + kmajor(kk), q_mn + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
+            mma_commit(bar(L::bStageEmpty + s));
+          }
+          __syncwarp();
+        }
+        if (it + 1 < n_iter) {
+          if (!(ok = issue_dp(t + 1))) break;
+          if (it + 2 == n_iter) commit(L::bVFree);  // the item's last reader of V
+        }
+      }
+      if (!ok) break;
+      commit(L::bFinal);
+      g += n_iter;
     }
     if (*abort_flag) {
       if (elect_one()) {
@@ -424,16 +526,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int grp = warp >= 10;  // query columns [64 grp, 64 grp + 64) of each key row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int kr = (warp & 3) * 32 + lane;  // key row within the tile
-    const int key = n * kTile + kr;
-    const bool key_ok = key < p.N;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    uint32_t pk[2][16];  // this warp's half of P_it^T as packed bf16, kept for the dS phase
-    // P phase of query tile `it`: P^T = 2^(S^T scale log2e - LSE2), bf16 into TMEM and pk.
+    uint32_t pk[2][16];  // this warp's half of P_t^T as packed bf16, kept for the dS phase
+    int g = 0;           // query tiles of earlier items
+    for (int r = 0; ok; ++r) {
+    const int idx = take_item(r);
+    if (idx < 0) break;
+    const BwdItem w = bwd_item<kWin>(idx, p);
+    const int n = w.n, n_iter = w.n_iter;
+    const int key = n * kTile + kr;
+    const bool key_ok = key < p.N;
+    // P phase of the item's query tile `it` (tile t = g + it of the CTA):
+    // P^T = 2^(S^T scale log2e - LSE2), bf16 into TMEM and pk.
     auto p_phase = [&](int it) -> bool {
-      const int s = it & 1;
-      int hq, i;
-      item(it, hq, i);
+      const int t = g + it;
+      const int s = t & 1;
+      const int i = w.i0 + it % w.n_i;
       const bool diag = p.causal && i == n;
       // Window: query q sees key j only if q - j < window; (i - n) * 128 + q - kr is q - j.
       const bool wmask = kWin && (i - n) * kTile + kTile - 1 >= p.window;
@@ -442,8 +551,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q_lo = !key_ok ? kTile : (diag ? kr : 0);
       const int q_hi = wmask ? kr + p.window - 1 - (i - n) * kTile : kTile - 1;
       const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < kTile - 1);  // warp-uniform
-      if (!mbar_wait_warp(bar(L::bQFull + s), (it >> 1) & 1, ctl)) return false;
-      if (!mbar_wait_warp(bar(L::bSFull), it & 1, ctl)) return false;
+      if (!mbar_wait_warp(bar(L::bQFull + s), (t >> 1) & 1, ctl)) return false;
+      if (!mbar_wait_warp(bar(L::bSFull), t & 1, ctl)) return false;
       tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -486,12 +595,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar(L::bPReady));
       return true;
     };
-    ok = n_iter > 0 && p_phase(0);
+    ok = p_phase(0);
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it & 1;
+      const int t = g + it;
+      const int s = t & 1;
       const float* sd = reinterpret_cast<const float*>(stage_ptr(s) + L::kStD);
-      if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), (it >> 1) & 1, ctl))) break;
-      if (!(ok = mbar_wait_warp(bar(L::bDPFull), it & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bDOFull + s), (t >> 1) & 1, ctl))) break;
+      if (!(ok = mbar_wait_warp(bar(L::bDPFull), t & 1, ctl))) break;
       tc_fence_after();
       // dS^T = P^T (dP^T - delta) with the bf16 P the dV MMA used. dS goes to shared memory
       // only after dV_it (issued after dP_it) has read the dO slot it reuses (d = 128), and
@@ -518,7 +628,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds[j / 2 + 1] = pack_bf16(s23.x, s23.y);
         }
         // dS takes dO_it's slot (d = 128): dV_it, issued after dP_it, must have read it.
-        if (cc == 0 && !(ok = mbar_wait_warp(bar(L::bDVDone), it & 1, ctl))) break;
+        if (cc == 0 && !(ok = mbar_wait_warp(bar(L::bDVDone), t & 1, ctl))) break;
         // Shared-memory copy of dS: row = key, 64-query chunks 16 KB apart, 16-byte granules
         // (8 queries) XOR-swizzled by (key mod 8): the MN-major A operand of the dQ MMA.
 #pragma unroll
@@ -534,69 +644,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar(L::bSmemDS));
       if (it + 1 < n_iter && !(ok = p_phase(it + 1))) break;
     }
-    // ---------------------------------------------------------------- dV (0-3) / dK (10-13) epilogue
-    if (ok) ok = mbar_wait_warp(bar(L::bFinal), 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      const uint32_t src = grp ? tdK : tdV;
-      const float mul = grp ? p.scale : 1.f;
-      if (n_iter <= kBwdStoreViaTmaMaxIter) {
-        // A short CTA's epilogue is a noticeable part of its time: every MMA has completed, so the
-        // Q/dO stages are idle, and warp w of the dV (dK) warps writes its 32 key rows, one
-        // 64-column chunk at a time, into an 8 KB region of stage 0 (1) in the 128-byte swizzled
-        // order; one lane stores each chunk with a bulk tensor store (whole lines; rows past N are
-        // not written). Measured +9 % on the backward at N = 512 and +3.6 % at B=4 H=16 N=4096
-        // causal. A long CTA stores its rows directly and leaves the TMA unit to its dQ
-        // reductions (the same speed on CTAs of 128 query tiles; this build, with both paths,
-        // also ran ~2 % faster there than one with the bulk path alone).
-        const uint32_t buf = stage(grp) + (uint32_t)(warp & 3) * 8192;
-        const int y0 = n * kTile + (warp & 3) * 32;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t a[2][32];
-          tmem_ld32(src + lane_off + (2 * c) * 32, a[0]);
-          tmem_ld32(src + lane_off + (2 * c + 1) * 32, a[1]);
-          tmem_ld_wait(a[0]);
-          tmem_ld_wait(a[1]);
-          const uint32_t cb = buf + (uint32_t)c * 4096;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint32_t* v = a[g >> 2] + 8 * (g & 3);
-            st_shared_v4(cb + (uint32_t)lane * 128 + ((g ^ (lane & 7)) << 4),
-                         pack_bf16(__uint_as_float(v[0]) * mul, __uint_as_float(v[1]) * mul),
-                         pack_bf16(__uint_as_float(v[2]) * mul, __uint_as_float(v[3]) * mul),
-                         pack_bf16(__uint_as_float(v[4]) * mul, __uint_as_float(v[5]) * mul),
-                         pack_bf16(__uint_as_float(v[6]) * mul, __uint_as_float(v[7]) * mul));
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && y0 < p.N) {
-            tma_store_3d(grp ? &tm_dk : &tm_dv, cb, c * 64, y0, b * p.Hkv + hkv);
-            bulk_commit_group();
-          }
-        }
-        if (lane == 0) bulk_wait_read_all();  // the stores have read their shared memory
-      } else {
-        const size_t row_off = ((size_t)(b * p.Hkv + hkv) * p.N + key) * D;
-        __nv_bfloat16* dst_base = grp ? p.dk : p.dv;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(src + lane_off + c * 32, a);
-          tmem_ld_wait(a);
-          uint4 w[4];
-          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            wp[j] = pack_bf16(__uint_as_float(a[2 * j]) * mul, __uint_as_float(a[2 * j + 1]) * mul);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_base + row_off + c * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = w[j];
-          }
-        }
-      }
-    }
+    g += n_iter;
+    }  // items
   } else {
     // ------------------------------------------------------------------ dQ drain warps 6-9
     // Each warp owns 32 query rows (its TMEM lane quarter). 32 columns at a time, the warp
@@ -605,12 +654,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // bulk tensor reduction. Warps never wait for one another.
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t stage_buf = sbase + L::kDQ + (uint32_t)(warp & 3) * 8192;
-    for (int it = 0; it < n_iter; ++it) {
-      int hq, i;
-      item(it, hq, i);
-      if (!mbar_wait_warp(bar(L::bDQFull), it & 1, ctl)) break;
+    bool ok = true;
+    int t = 0;  // query tiles drained (all items)
+    for (int r = 0; ok; ++r) {
+    const int idx = take_item(r);
+    if (idx < 0) break;
+    const BwdItem w = bwd_item<kWin>(idx, p);
+    for (int it = 0; it < w.n_iter; ++it, ++t) {
+      const int gi = it / w.n_i;
+      const int hq = w.hkv * G + gi;
+      const int i = w.i0 + (it - gi * w.n_i);
+      if (!(ok = mbar_wait_warp(bar(L::bDQFull), t & 1, ctl))) break;
       tc_fence_after();
-      const int row0 = (b * p.Hq + hq) * p.Npad + i * kTile + (warp & 3) * 32;
+      const int row0 = (w.b * p.Hq + hq) * p.Npad + i * kTile + (warp & 3) * 32;
       // Two halves of 64 columns (the register budget of 14 warps), each chunk staged through
       // buffer (chunk mod 2): a buffer is rewritten only after the reduction issued from it
       // two chunks earlier has read it, so the first half never waits for a reduction and the
@@ -645,6 +701,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
+    if (!ok) break;
+    // ---------------------------------------------------------------- dV / dK epilogue
+    // Once every MMA of the item has completed, the drain warp moves its 32 key rows of dV,
+    // then dK, out of TMEM 64 columns at a time, releases the accumulator columns after the last
+    // read (the next item's first dV / dK MMA may then start), and writes each chunk as bf16
+    // through its staging buffers with a bulk tensor store (whole lines; rows past N are not
+    // written). The softmax warps meanwhile start on the next item.
+    if (!(ok = mbar_wait_warp(bar(L::bFinal), r & 1, ctl))) break;
+    tc_fence_after();
+    {
+      const int y0 = w.n * kTile + (warp & 3) * 32;
+      const int kv_z = w.b * p.Hkv + w.hkv;
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        const uint32_t src = grp ? tdK : tdV;
+        const float mul = grp ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t a[2][32];
+          tmem_ld32(src + lane_off + (2 * c) * 32, a[0]);
+          tmem_ld32(src + lane_off + (2 * c + 1) * 32, a[1]);
+          tmem_ld_wait(a[0]);
+          tmem_ld_wait(a[1]);
+          if (grp == 1 && c == D / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(L::bAccFree));
+          }
+          // Chunks alternate between the two buffers (dV then dK at d = 64).
+          const uint32_t buf = stage_buf + (uint32_t)((grp * (D / 64) + c) & 1) * 4096;
+          if (lane == 0) bulk_wait_read_but1();  // the copy issued from this buffer has read it
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* v = a[q >> 2] + 8 * (q & 3);
+            st_shared_v4(buf + (uint32_t)lane * 128 + ((q ^ (lane & 7)) << 4),
+                         pack_bf16(__uint_as_float(v[0]) * mul, __uint_as_float(v[1]) * mul),
+                         pack_bf16(__uint_as_float(v[2]) * mul, __uint_as_float(v[3]) * mul),
+                         pack_bf16(__uint_as_float(v[4]) * mul, __uint_as_float(v[5]) * mul),
+                         pack_bf16(__uint_as_float(v[6]) * mul, __uint_as_float(v[7]) * mul));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (y0 < p.N) tma_store_3d(grp ? &tm_dk : &tm_dv, buf, c * 64, y0, kv_z);
+            bulk_commit_group();
+          }
+        }
+      }
+    }
+    }  // items
     if (lane == 0) bulk_wait_all();  // every reduction has landed before the CTA exits
   }
 
@@ -696,7 +802,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     fa_bwd_pre_kernel<D><<<blocks, 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.dq_acc,
-        a.delta, a.lse2, a.N, Npad, rows);
+        a.delta, a.lse2, a.next_item, a.N, Npad, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -724,7 +830,10 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * kLog2e;
     p.band = bwd_band(a.B, a.Hq, a.Hkv, a.N, D, a.causal, a.window, a.num_sms);
-    const long long grid = (long long)a.B * a.Hkv * T;
+    p.num_items = a.B * a.Hkv * T;
+    p.next_item = a.next_item;
+    // Persistent: one CTA per SM (fewer if there are fewer items).
+    const long long grid = std::min<long long>(p.num_items, a.num_sms);
     kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, *a.tm_dk,
                                                           *a.tm_dv, p);
     e = cudaGetLastError();

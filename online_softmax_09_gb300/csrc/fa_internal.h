@@ -57,6 +57,7 @@ struct BwdLaunch {
   float* dq_acc;   // workspace: [B*Hq][Npad][d] fp32
   float* delta;    // workspace: [B*Hq][Npad] fp32
   float* lse2;     // workspace: [B*Hq][Npad] fp32 (LSE * log2 e; +inf on padded rows)
+  uint32_t* next_item;  // workspace: work-item counter of the main kernel (zeroed by prepare)
   uint32_t* status;
   int B, Hq, Hkv, N, d, causal;
   int window;  // 0: none; > 0: causal sliding window
