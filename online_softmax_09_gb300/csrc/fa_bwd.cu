@@ -199,12 +199,13 @@ struct BwdSmem {
     bDVDone,  // dV_i has finished reading dO_i (whose slot then takes dS_i)
     bDQFull,
     bDQFree,
-    bFinal,   // every MMA of the item has completed: dK, dV final in TMEM, K no longer read
+    bFinal,   // every MMA of the item has completed: dK, dV final in TMEM
+    bKFree,   // the item's last dQ MMA has read K
     bVFree,   // the item's last dP^T MMA has read V
     bAccFree, // the epilogue has read dK and dV out of TMEM
-    bItemFull = 18,   // 2
-    bItemEmpty = 20,  // 2
-    bDrain = 22,
+    bItemFull = 19,   // 2
+    bItemEmpty = 21,  // 2
+    bDrain = 23,
     kNumBars
   };
   static_assert(bDOFull == bQFull + 2 && bStageEmpty == bDOFull + 2 && bSFull == bStageEmpty + 2 &&
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(L::bDVDone), 1);
     mbar_init(bar(L::bDQFree), 128);
     mbar_init(bar(L::bFinal), 1);
+    mbar_init(bar(L::bKFree), 1);
     mbar_init(bar(L::bVFree), 1);
     mbar_init(bar(L::bAccFree), 128);
     mbar_init(bar(L::bDrain), 1);
@@ -344,6 +346,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx < 0) break;
         const BwdItem w = bwd_item<kWin>(idx, p);
         const int kv_z = w.b * p.Hkv + w.hkv;
+        if (r > 0) {  // K and V into L2 now; into shared memory once the previous item frees them
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_l2_3d(&tm_k, c * 64, w.n * kTile, kv_z);
+            tma_prefetch_l2_3d(&tm_v, c * 64, w.n * kTile, kv_z);
+          }
+        }
         auto load_tile = [&](int it) -> bool {
           const int s = g & 1;
           if (!mbar_wait(bar(L::bStageEmpty + s), ((g >> 1) & 1) ^ 1, ctl)) return false;
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sV + c * 16384, &tm_v, bar(L::bV), c * 64, w.n * kTile, kv_z);
         v_loads = r + 1;
         if (w.n_iter > 0 && !(ok = load_tile(0))) break;
-        if (r > 0 && !(ok = mbar_wait(bar(L::bFinal), (r - 1) & 1, ctl))) break;
+        if (r > 0 && !(ok = mbar_wait(bar(L::bKFree), (r - 1) & 1, ctl))) break;
         mbar_expect_tx(bar(L::bK), kTB);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
@@ -498,6 +507,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_ss(tdP, ds_mn + (uint32_t)(kk * (2048 >> 4)), dK_mn + (uint32_t)(kk * (2048 >> 4)), idDQ,
                      kk > 0);
             mma_commit(bar(L::bDQFull));
+            if (it + 1 == n_iter) mma_commit(bar(L::bKFree));  // the item's last reader of K
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_ss(tdK, ds_k + kmajor(kk), q_mn + (uint32_t)(kk * (2048 >> 4)), idTS, (it > 0 || kk > 0));
