@@ -114,6 +114,26 @@ def test_dk_dv_deterministic_and_workspace_reuse():
     assert rel_fro(g2[0].float().cpu().numpy(), g1[0].float().cpu().numpy()) < 1e-2
 
 
+@pytest.mark.parametrize("shape", [(8, 4, 4, 1024, 128), (4, 8, 2, 3000, 64)])
+def test_compute_stage_runs_again_without_a_new_prepare(shape):
+    # The compute kernel hands out work items from a workspace counter and leaves it at zero,
+    # so a second compute after one prepare redoes every item: dK and dV come out the same bit
+    # for bit, and the dQ accumulator holds every contribution twice. Shapes with more work
+    # items than SMs, so CTAs take several items each.
+    fa = fa_mod()
+    B, Hq, Hkv, N, d = shape
+    q, k, v, do = (t.cuda() for t in make_qkv(B, Hq, Hkv, N, d, seed=10 + N, with_do=True))
+    o, lse = fa.forward(q, k, v, True)
+    ref = [t.clone() for t in fa.backward(q, k, v, o, do, lse, True)]
+    ws = torch.empty(fa.workspace_bytes(B, Hq, Hkv, N, d), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa.backward_stages(q, k, v, o, do, lse, dq, dk, dv, ws, True, only=(0, 1))
+    fa.backward_stages(q, k, v, o, do, lse, dq, dk, dv, ws, True, only=(1, 2))
+    fa.check()
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert rel_fro(dq.float().cpu().numpy(), 2 * ref[0].float().cpu().numpy()) < 1e-2
+
+
 def test_backward_workspace_has_no_n_squared_term():
     fa = fa_mod()
     sizes = [fa.workspace_bytes(1, 32, 8, n, 128) for n in (4096, 8192, 16384)]
