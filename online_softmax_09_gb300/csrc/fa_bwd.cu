@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // in launch order, so items still start in the order a one-CTA-per-item launch would start
     // them (and the band order holds). Each item is published to the other roles through a
     // two-slot ring. V of the next item is loaded once the previous item's last dP^T MMA has
-    // read V, K once all its MMAs are done; Q, dO, LSE2 and delta go through the two stages.
+    // read V, K once its last dQ MMA has read K (both are prefetched into L2 when the item is
+    // fetched); Q, dO, LSE2 and delta go through the two stages.
     if (lane == 0) {
       constexpr uint32_t kTB = L::kTileBytes;
       int g = 0;        // query tiles loaded so far (all items)
@@ -773,9 +774,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// (b, kv head) pairs per launch band. Bands shrink the set of heads whose Q, dO and fp32 dQ
-// accumulator rows the resident CTAs share: as many bands as keep each band's work per SM at
-// least 1.4 times its longest CTA (whose G * T query tiles would otherwise end alone; a
+// (b, kv head) pairs per band of work items. Bands shrink the set of heads whose Q, dO and fp32
+// dQ accumulator rows the items in flight share: as many bands as keep each band's work per SM
+// at least 1.4 times its longest item (whose G * T query tiles would otherwise end alone; a
 // measured margin: 1.28 lost 3 %, 1.41 and above gained), but no more than it takes to fit a
 // band's working set (its G query heads' Q and dO, bf16, and dQ accumulator, fp32, plus K and
 // V) in about 80 MiB of the 129 MB L2. One band (plain key-tile-major order) where the margin
@@ -787,7 +788,7 @@ static int bwd_band(int B, int Hq, int Hkv, int N, int d, int causal, int window
   if (window > 0 || num_sms < 1) return BHk;
   const double ws = (double)N * d * (8.0 * G + 4.0);
   const int kb_l2 = std::max(1, (int)(80.0 * 1024.0 * 1024.0 / ws));
-  // Work of one (b, kv head) in query-tile iterations, over its longest CTA's: (T + 1) / 2
+  // Work of one (b, kv head) in query-tile iterations, over its longest item's: (T + 1) / 2
   // causal, T non-causal.
   const double ratio = causal ? (T + 1) / 2.0 : (double)T;
   const int kb_tail = (int)std::ceil(1.4 * num_sms / ratio);
