@@ -126,14 +126,13 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
 struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  float* dq_acc;
   const float* delta;
   const float* lse2;
   uint32_t* status;
   int B, Hq, Hkv, N, Npad, causal, num_tiles;
   int window;  // > 0: causal sliding window of this many keys
   float scale, scale_log2;
-  int band;       // (b, kv head) pairs per launch band; B * Hkv for a single band
+  int band;       // (b, kv head) pairs per band of work items; B * Hkv for a single band
   int num_items;  // B * Hkv * num_tiles work items (key tiles)
   uint32_t* next_item;  // workspace: [0] items handed out beyond the first gridDim.x,
                         // [1] CTAs that found no more items
@@ -183,7 +182,8 @@ struct BwdSmem {
   static constexpr int kStD = 2 * kTileBytes + 512;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kDS = kStage0 + 2 * kStageBytes;
-  // dQ staging for the bulk reductions: 4 drain warps x 2 buffers x 32 rows x 128 bytes.
+  // dQ staging for the bulk reductions (and, at an item's end, the dK / dV bulk stores):
+  // 4 drain warps x 2 buffers x 32 rows x 128 bytes.
   static constexpr int kDQ = kDS + (kAliasDS ? 0 : kTile * kTile * 2);
   static constexpr int kBar = kDQ + 4 * 2 * 32 * 128;
   enum {
@@ -826,7 +826,6 @@ static cudaError_t launch_bwd_t(const BwdLaunch& a, int stages) {
     BwdParams p;
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
-    p.dq_acc = a.dq_acc;
     p.delta = a.delta;
     p.lse2 = a.lse2;
     p.status = a.status;
