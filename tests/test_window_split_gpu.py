@@ -131,3 +131,30 @@ def test_window_backward_long_sequence_sampled():
         rk, rv = rk + gk, rv + gv
     assert_grad_close("dk", dk[0, 1, idx].float().cpu().numpy(), rk, what="window=1000 sampled")
     assert_grad_close("dv", dv[0, 1, idx].float().cpu().numpy(), rv, what="window=1000 sampled")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_backward_more_items_than_sms(d):
+    # 4 x 4 kv heads x 16 key tiles = 256 work items for 152 CTAs: most CTAs take two window
+    # items, so the persistent backward's item hand-over runs in window mode too. Checked on
+    # sampled rows of the last batch element's kv head 3 (query heads 6, 7).
+    from gpu_util import assert_grad_close
+
+    fa = fa_mod()
+    B, Hq, Hkv, N, w = 4, 8, 4, 2048, 300
+    q, k, v, do = make_qkv(B, Hq, Hkv, N, d, seed=45 + d, value_scale=0.5, with_do=True)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.forward_window(qd, kd, vd, w)
+    dq, dk, dv = fa.backward_window(qd, kd, vd, o, dod, lse, w)
+    fa.check()
+    rows = sample_rows(N, 24, seed=45) + [0, 127, 128, 299, 300, 2047]
+    idx = torch.as_tensor(rows, device="cuda")
+    b, hk, scale = B - 1, Hkv - 1, 1 / math.sqrt(d)
+    rk = rv = 0
+    for hq in (2 * hk, 2 * hk + 1):
+        a = (to_f64(q[b, hq]), to_f64(k[b, hk]), to_f64(v[b, hk]), to_f64(do[b, hq]))
+        rq, gk, gv = oracle.attention_backward_rows(*a, rows, rows, True, scale, window=w)
+        assert_grad_close("dq", dq[b, hq, idx].float().cpu().numpy(), rq, what=f"window={w} head {hq}")
+        rk, rv = rk + gk, rv + gv
+    assert_grad_close("dk", dk[b, hk, idx].float().cpu().numpy(), rk, what=f"window={w}")
+    assert_grad_close("dv", dv[b, hk, idx].float().cpu().numpy(), rv, what=f"window={w}")
