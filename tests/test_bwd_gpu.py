@@ -140,3 +140,32 @@ def test_backward_workspace_has_no_n_squared_term():
     assert sizes[2] - sizes[1] == 2 * (sizes[1] - sizes[0])
     # fp32 dQ accumulator + two fp32 row statistics + one 256-byte work counter, nothing else.
     assert sizes[0] == 32 * 4096 * (128 + 2) * 4 + 256
+
+
+def _random_configs(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        hkv = int(rng.choice([1, 2, 3, 4]))
+        g = int(rng.choice([1, 2]))
+        out.append((int(rng.integers(1, 17)), hkv * g, hkv, int(rng.integers(1, 800)), int(rng.choice([64, 128])),
+                    bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", _random_configs(8, seed=2267))
+def test_random_shapes_forward_and_backward(B, Hq, Hkv, N, d, causal):
+    # Seeded random batch, GQA ratio, ragged N, head dim and mask (this seed gives three shapes
+    # with more backward work items than SMs): the forward and the persistent backward in full
+    # against the oracle.
+    q, k, v, do = make_qkv(B, Hq, Hkv, N, d, seed=7000 + N, with_do=True)
+    scale = 1 / math.sqrt(d)
+    o, lse, dq, dk, dv = gpu_fwd_bwd(q, k, v, do, causal)
+    O_ref, L_ref = oracle.attention_forward(to_f64(q), to_f64(k), to_f64(v), causal, scale)
+    from gpu_util import assert_fwd_close
+    assert_fwd_close(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref, "random shape")
+    ref = oracle.attention_backward(to_f64(q), to_f64(k), to_f64(v), to_f64(do), causal, scale)
+    fro_floor = 1e-3 * np.linalg.norm(ref[2])
+    max_floor = 1e-3 * float(np.max(np.abs(ref[2])))
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        assert_grad_close(name, g.float().cpu().numpy(), r, fro_floor, max_floor, what="random shape")
